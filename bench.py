@@ -1,0 +1,451 @@
+"""Benchmark one continuous-batching paged-attention step through libcb's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config decode|mixed|long_decode|long_decode_window|tiny_mixed]
+
+A step is the whole hot path on one synthetic batch: scatter of the step's new
+K/V through slot_mapping, then paged attention of every query row (decode and
+prefill rows). The default workload is the pure-decode step: 64 requests,
+q_len 1, seq_len ~ U{128..2048}, 32 Q / 8 KV heads, head_dim 128,
+block_size 16, bf16.
+
+Reported metric: achieved KV-read HBM bandwidth (algorithmic KV bytes of the
+step, every attended position of every request counted once, over the step's
+device time) and query tokens/s, with the roofline of the dominant kernel
+against the measured HBM copy bandwidth. L2 is flushed (a 512 MiB write)
+between timed steps. With N > 1 (torchrun), every rank runs an independent
+replica of the step (the path needs no exchange) and the job value is the sum
+of the bytes over the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (float64 NumPy, as it stands) on the
+same workload instead, on the host cores.
+"""
+from __future__ import annotations
+
+import os
+
+# the oracle leg is timed single-threaded; set before numpy loads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- accounting
+
+
+def kv_bytes(spec) -> int:
+    """Algorithmic KV bytes: every attended position of every request once, K and V."""
+    return spec.kv_tokens_attended() * 2 * spec.num_kv_heads * spec.head_dim * spec.elt_bytes()
+
+
+def decode_kernel_bytes(spec) -> int:
+    """Algorithmic bytes of the decode kernel: decode rows' KV + their q and out."""
+    e = spec.elt_bytes()
+    n = 0
+    for r in range(spec.R):
+        if int(spec.q_lens[r]) != 1:
+            continue
+        ctx = int(spec.ctx_lens[r])
+        lo = 0 if spec.sliding_window <= 0 else max(0, ctx - spec.sliding_window + 1)
+        n += (ctx - lo + 1) * 2 * spec.num_kv_heads * spec.head_dim * e
+        n += 2 * spec.num_q_heads * spec.head_dim * e
+    return n
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    src = os.path.join(ROOT, "paged_kv_attention_cb_gb300", "csrc", name)
+    try:
+        with open(src, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return ""
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha") != kernel_source_sha(rec["source"]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1].split()[0]))
+                    mx.append(float(parts[2].split()[0]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo", init_method="env://")
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, spec, world, rank, local):
+    import torch
+
+    import paged_kv_attention_cb_gb300 as cb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = workloads.draw_tensors(spec, dev)
+    md = workloads.metadata_tensors(spec, dev)
+    ws = cb.alloc_workspace(spec.R, spec.T, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                            dev)
+    out = torch.empty_like(x["q"])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cb.paged_attention(out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
+                           md["seq_lens"], md["block_table"], spec.query_start_loc,
+                           spec.seq_lens, ws, scale=spec.scale,
+                           sliding_window=spec.sliding_window, k_new=x["k_new"],
+                           v_new=x["v_new"], slot_mapping=md["slot_mapping"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if cb.read_error_word(ws) != 0:
+        raise RuntimeError("device bounds check fired during warm-up")
+
+    # ---- timed region: per-step CUDA events on the launching stream, L2 flushed between steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = cb.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            stops[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = cb.launch_count() - launches0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    local_ms = sum(step_ms)
+    total_ms = reduce_max(local_ms, world)
+    ms_per_step = total_ms / args.steps
+
+    # ---- per-kernel attribution pass (same steps, events around each launch)
+    cb.kernel_timing(True)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step()
+    per_kernel = cb.kernel_timing_collect()
+    cb.kernel_timing(False)
+
+    # ---- end to end through the public API: pinned host inputs in, result out
+    host_in = {k: v.cpu().pin_memory() for k, v in (("q", x["q"]), ("k_new", x["k_new"]),
+                                                     ("v_new", x["v_new"]))}
+    host_md = {k: v.cpu().pin_memory() for k, v in md.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    dev_md = {k: torch.empty_like(v, device=dev) for k, v in host_md.items()}
+    h2d = sum(v.numel() * v.element_size() for v in list(host_in.values()) + list(host_md.values()))
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        for k in dev_md:
+            dev_md[k].copy_(host_md[k], non_blocking=True)
+        cb.paged_attention(out, dev_in["q"], x["k_cache"], x["v_cache"],
+                           dev_md["query_start_loc"], dev_md["seq_lens"], dev_md["block_table"],
+                           spec.query_start_loc, spec.seq_lens, ws, scale=spec.scale,
+                           sliding_window=spec.sliding_window, k_new=dev_in["k_new"],
+                           v_new=dev_in["v_new"], slot_mapping=dev_md["slot_mapping"],
+                           stream=stream)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e_starts[i].record(stream)
+        e2e_step()
+        e_stops[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world)
+    barrier(world)
+    return dict(ms_per_step=ms_per_step, step_ms=step_ms, launches=launches,
+                per_kernel=per_kernel, e2e_ms_per_step=e2e_ms / args.steps, h2d=h2d, d2h=d2h,
+                clocks=clocks.summary())
+
+
+# ---------------------------------------------------------------- oracle
+
+
+def oracle_inputs(spec):
+    """Host float64-ready copies of the step's seeded inputs (CPU torch generator)."""
+    x = workloads.draw_tensors(spec, "cpu")
+    f = lambda t: t.float().numpy()
+    return {k: f(v) for k, v in x.items()}
+
+
+def time_oracle(spec, budget_s: float, h=None, max_steps=None):
+    """Run whole oracle steps (scatter + attention) until the time budget is spent."""
+    import oracle
+
+    if h is None:
+        h = oracle_inputs(spec)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.step(h["q"], h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], spec.slot_mapping,
+                    spec.query_start_loc, spec.seq_lens, spec.block_table, spec.block_size,
+                    spec.scale, spec.sliding_window)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and done >= max_steps):
+            return done, el
+
+
+def oracle_sample_spec(spec, max_requests=None):
+    """A bounded sample of the workload for the oracle: the first requests of the step."""
+    if max_requests is None or max_requests >= spec.R:
+        return spec, "whole step"
+    r = max_requests
+    s = workloads.StepSpec(**{**spec.__dict__})
+    s.q_lens = spec.q_lens[:r]
+    s.ctx_lens = spec.ctx_lens[:r]
+    s.query_start_loc = spec.query_start_loc[:r + 1]
+    s.seq_lens = spec.seq_lens[:r]
+    s.block_table = spec.block_table[:r]
+    s.slot_mapping = spec.slot_mapping[:int(spec.query_start_loc[r])]
+    return s, f"first {r} of {spec.R} requests"
+
+
+def oracle_sample_size(config):
+    # requests per oracle sample so that one sample takes a few seconds at most
+    return {"decode": None, "tiny_mixed": None, "mixed": 24, "long_decode": 2,
+            "long_decode_window": 8}.get(config)
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline figure")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world, rank, local = dist_setup()
+    spec = workloads.by_name(args.config)
+    kvb = kv_bytes(spec)
+    metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
+    cfg = {"workload": spec.name, "requests": spec.R, "query_tokens": spec.T,
+           "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+           "head_dim": spec.head_dim, "block_size": spec.block_size,
+           "num_blocks": spec.num_blocks, "sliding_window": spec.sliding_window,
+           "kv_bytes_per_step": kvb, "l2": "flushed (512 MiB write) between timed steps",
+           "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample, what = oracle_sample_spec(spec, oracle_sample_size(args.config))
+        h = oracle_inputs(sample)
+        for _ in range(args.warmup):
+            time_oracle(sample, 0.0, h, max_steps=1)
+        per = []
+        for _ in range(args.steps):
+            n, el = time_oracle(sample, 0.0, h, max_steps=1)
+            per.append(el)
+        t = sum(per)
+        sb = kv_bytes(sample) * args.steps
+        val = sb / t / 1e9
+        line = {"impl": "reference", "metric": metric, "value": val, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg,
+                "tokens_per_s": sample.T * args.steps / t,
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{what}, one oracle step per timed step"},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    res = run_ours(args, spec, world, rank, local)
+    if rank != 0:
+        return
+    ms = res["ms_per_step"]
+    value = world * kvb / (ms * 1e-3) / 1e9
+    tok_s = world * spec.T / (ms * 1e-3)
+    peak, peak_kind = peaks()
+
+    # dominant kernel: most device time in the attribution pass
+    pk = res["per_kernel"]
+    dom = max(pk.items(), key=lambda kv: kv[1][0])[0] if pk else None
+    dom_ms = pk[dom][0] / pk[dom][1] if dom else None
+    if dom == "decode_split":
+        dom_bytes, src = decode_kernel_bytes(spec), "attn_decode.cu"
+    elif dom == "portable_attention":
+        dom_bytes, src = kvb + 2 * spec.T * spec.num_q_heads * spec.head_dim * spec.elt_bytes(), \
+            "attn_portable.cu"
+    else:
+        dom_bytes, src = kvb, ""
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "avg_launch_ms": dom_ms,
+                "traffic": recorded_traffic(dom, spec.name) if dom else None}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sample, what = oracle_sample_spec(spec, oracle_sample_size(args.config))
+        n, el = time_oracle(sample, args.cpu_budget)
+        cpu = {"value": kv_bytes(sample) * n / el / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{what} x {n} oracle steps in {el:.1f} s"}
+
+    e2e_ms = res["e2e_ms_per_step"]
+    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if spec.dtype == "bf16" else "f32", "data": "synthetic", "config": cfg,
+            "tokens_per_s": tok_s,
+            "step_ms_median": statistics.median(res["step_ms"]),
+            "e2e": {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": res["launches"],
+            "per_kernel_ms": {k: v[0] / v[1] for k, v in pk.items()},
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": res["clocks"]}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

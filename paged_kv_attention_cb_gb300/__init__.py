@@ -1,0 +1,200 @@
+"""Python binding of libcb (C ABI in include/cb.h): argument marshalling only.
+
+Every step of the attention path runs in the library's CUDA kernels; this
+module only turns torch tensors into device pointers and sizes, passes the
+caller's current CUDA stream, and raises ``CbError`` on a non-OK status. If
+libcb.so has not been built, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH
+
+CB_F32 = 0
+CB_BF16 = 1
+CB_FLAG_PORTABLE_ONLY = 0x1
+
+STATUS = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_METADATA", 3: "CB_ERR_UNSUPPORTED",
+          4: "CB_ERR_WORKSPACE", 5: "CB_ERR_CUDA", 6: "CB_ERR_DEVICE_CHECK"}
+
+
+class CbError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_LIB = None
+
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+_SIGNATURES = {
+    "cb_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "cb_last_error_message": (ctypes.c_char_p, []),
+    "cb_last_cuda_error": (ctypes.c_int, []),
+    "cb_abi_version": (ctypes.c_int, []),
+    "cb_write_kv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                   _vp, _vp]),
+    "cb_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
+    "cb_workspace_init": (ctypes.c_int, [_vp, ctypes.c_size_t, _vp]),
+    "cb_paged_attention": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp,            # out, q, k_cache, v_cache
+        _vp, _vp, _vp,                 # k_new, v_new, slot_mapping
+        _vp, _vp, _vp, _i32,           # query_start_loc, seq_lens, block_table, stride
+        _vp, _vp,                      # host mirrors
+        _i32, _i32, _i32, _i32,        # R, T, num_blocks, block_size
+        _i32, _i32, _i32,              # Hq, Hkv, D
+        ctypes.c_float, _i32, _i32,    # scale, sliding_window, dtype
+        ctypes.c_uint32, _vp, ctypes.c_size_t, _vp]),  # flags, workspace, bytes, stream
+    "cb_read_error_word": (ctypes.c_int, [_vp, _vp, _vp]),
+    "cb_launch_count": (ctypes.c_longlong, [ctypes.c_int]),
+    "cb_num_kernels": (ctypes.c_int, []),
+    "cb_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "cb_kernel_timing": (ctypes.c_int, [ctypes.c_int]),
+    "cb_kernel_timing_collect": (ctypes.c_int, [_vp, _vp, ctypes.c_int]),
+}
+
+
+def lib_path() -> str:
+    return os.environ.get("CB_LIB", LIB_PATH)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libcb.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libcb.so not built at {path}: run paged_kv_attention_cb_gb300.build")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def _check(status: int):
+    if status != 0:
+        msg = lib().cb_last_error_message().decode()
+        raise CbError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return CB_F32
+    if t.dtype == torch.bfloat16:
+        return CB_BF16
+    raise CbError(1, f"unsupported dtype {t.dtype}")
+
+
+def _host_i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, error_word=None, stream=None):
+    """Scatter k_new/v_new [T, Hkv, D] into the caches [NB, BS, Hkv, D] at slot_mapping [T]."""
+    T, Hkv, D = k_new.shape
+    NB, BS = k_cache.shape[0], k_cache.shape[1]
+    _check(lib().cb_write_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                             _ptr(slot_mapping), T, NB, BS, Hkv, D, _dtype_code(k_new),
+                             _ptr(error_word), _stream(stream)))
+
+
+def workspace_size(num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(lib().cb_workspace_size(num_requests, num_tokens, num_q_heads, num_kv_heads,
+                                       head_dim))
+
+
+def workspace_init(workspace, stream=None):
+    _check(lib().cb_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)))
+
+
+def read_error_word(workspace, stream=None) -> int:
+    """Synchronise, return and clear the device error word (0 = no error recorded)."""
+    word = ctypes.c_int32(0)
+    status = lib().cb_read_error_word(_ptr(workspace), ctypes.byref(word), _stream(stream))
+    if status not in (0, 6):
+        _check(status)
+    return int(word.value)
+
+
+def paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                    h_query_start_loc, h_seq_lens, workspace, *, scale=0.0, sliding_window=0,
+                    k_new=None, v_new=None, slot_mapping=None, flags=0, stream=None):
+    """One ragged paged-attention step (see cb_paged_attention in include/cb.h).
+
+    out, q: [T, Hq, D]; caches [NB, BS, Hkv, D]; device metadata int32 (slot_mapping
+    int64); h_query_start_loc / h_seq_lens: host copies of the same metadata.
+    """
+    T, Hq, D = q.shape
+    NB, BS, Hkv, _ = k_cache.shape
+    R = int(seq_lens.shape[0])
+    hq = _host_i32(h_query_start_loc)
+    hs = _host_i32(h_seq_lens)
+    if hq.shape[0] != R + 1 or hs.shape[0] != R:
+        raise CbError(2, "host mirrors must have R+1 and R entries")
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    _check(lib().cb_paged_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+        _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride,
+        hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
+        R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def launch_count(kernel: int = -1) -> int:
+    """Kernels launched by libcb in this process (all kernels when kernel < 0)."""
+    return int(lib().cb_launch_count(kernel))
+
+
+def kernel_names():
+    n = lib().cb_num_kernels()
+    return [lib().cb_kernel_name(k).decode() for k in range(n)]
+
+
+def kernel_timing(enable: bool):
+    _check(lib().cb_kernel_timing(1 if enable else 0))
+
+
+def kernel_timing_collect():
+    """{kernel name: (total ms, launches)} since the previous collect (synchronises)."""
+    n = lib().cb_num_kernels()
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    _check(lib().cb_kernel_timing_collect(ms, cnt, n))
+    names = kernel_names()
+    return {names[k]: (float(ms[k]), int(cnt[k])) for k in range(n) if cnt[k]}
+
+
+def alloc_workspace(num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim, device="cuda"):
+    """Allocate (with torch) and zero a workspace of cb_workspace_size bytes."""
+    import torch
+
+    n = workspace_size(num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim)
+    return torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device=device)

@@ -1,0 +1,31 @@
+// Work partition of one step (host side): which kernel serves which query rows,
+// and how the decode rows' KV is split across CTAs.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace cb {
+
+constexpr size_t kWorkspaceHeaderBytes = 256;  // error word + reserved
+constexpr int kMaxDecodeCtas = 2048;           // upper bound on decode CTAs (workspace sizing)
+
+size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim);
+
+struct Plan {
+  int portable_mode;   // -1: none, 0: all rows, 1: decode rows, 2: prefill rows
+  bool fast_decode;    // decode rows on the split-KV tensor-core kernel
+  bool fast_prefill;   // prefill rows on the tcgen05 tile kernel
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
+               uint32_t flags, void* workspace, size_t workspace_bytes);
+
+cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream);
+
+}  // namespace cb

@@ -1,0 +1,129 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function include/cb.h declares, and rejects bad arguments and inconsistent
+metadata on the host before launching anything (no GPU needed: validation
+returns before the first CUDA call)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_attention_cb_gb300 as cb
+from paged_kv_attention_cb_gb300 import build as cbbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbbuild.build()
+    return cb.lib()
+
+
+def declared_functions():
+    names = []
+    for fname in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(cb_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("cb_write_kv", "cb_paged_attention", "cb_workspace_size",
+                     "cb_status_string", "cb_last_cuda_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_exports_are_plain_c_symbols(lib):
+    nm = os.popen(f"nm -D --defined-only {cbbuild.LIB_PATH}").read()
+    for n in declared_functions():
+        assert re.search(rf"\bT {n}$", nm, flags=re.M), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.cb_abi_version() == 1
+    for s in range(7):
+        assert lib.cb_status_string(s)
+    assert lib.cb_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_is_monotone(lib):
+    a = lib.cb_workspace_size(4, 10, 4, 2, 64)
+    b = lib.cb_workspace_size(64, 64, 32, 8, 128)
+    c = lib.cb_workspace_size(128, 64, 32, 8, 128)
+    assert 256 <= a < b < c
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def call_attention(lib, qsl, seq, *, T=None, R=None, NB=40, BS=16, Hq=4, Hkv=2, D=64, dtype=0,
+                   stride=None, ws_bytes=None, scale=0.0, window=0, workspace=FAKE, out=FAKE,
+                   hq_ptr=True):
+    qsl = np.ascontiguousarray(qsl, dtype=np.int32)
+    seq = np.ascontiguousarray(seq, dtype=np.int32)
+    R = len(seq) if R is None else R
+    T = int(qsl[-1]) if T is None else T
+    if stride is None:
+        stride = max(1, int(max((seq + BS - 1) // BS))) if len(seq) else 1
+    if ws_bytes is None:
+        ws_bytes = lib.cb_workspace_size(R, T, Hq, Hkv, D)
+    hq = qsl.ctypes.data_as(ctypes.c_void_p) if hq_ptr else None
+    return lib.cb_paged_attention(out, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, stride,
+                                  hq, seq.ctypes.data_as(ctypes.c_void_p), R, T, NB, BS, Hq, Hkv, D,
+                                  scale, window, dtype, 0, workspace, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(qsl=[1, 2], seq=[3]), 2),                    # query_start_loc[0] != 0
+    (dict(qsl=[0, 3, 2], seq=[5, 5]), 2),              # decreasing
+    (dict(qsl=[0, 4], seq=[3]), 2),                    # q_len > seq_len
+    (dict(qsl=[0, 2], seq=[40], stride=2), 2),         # stride < ceil(40/16)
+    (dict(qsl=[0, 2], seq=[4], T=3), 2),               # qsl[R] != T
+    (dict(qsl=[0, 2], seq=[4], D=96), 3),              # head_dim
+    (dict(qsl=[0, 2], seq=[4], Hq=6, Hkv=2), 3),       # G = 3
+    (dict(qsl=[0, 2], seq=[4], Hq=5, Hkv=2), 1),       # Hq % Hkv
+    (dict(qsl=[0, 2], seq=[4], BS=12), 3),             # block size not a power of two
+    (dict(qsl=[0, 2], seq=[4], dtype=7), 1),           # dtype
+    (dict(qsl=[0, 2], seq=[4], ws_bytes=16), 4),       # workspace too small
+    (dict(qsl=[0, 2], seq=[4], workspace=None), 4),    # no workspace
+    (dict(qsl=[0, 2], seq=[4], hq_ptr=False), 1),      # host mirror missing
+    (dict(qsl=[0, 2], seq=[4], out=None), 1),          # null out
+    (dict(qsl=[0, 2], seq=[4], NB=0), 1),              # empty pool
+])
+def test_host_validation_rejects(lib, kwargs, status):
+    assert call_attention(lib, **kwargs) == status
+    assert lib.cb_last_error_message()
+
+
+def test_empty_step_is_a_no_op(lib):
+    # T = 0: validated, nothing launched, OK without a GPU.
+    assert call_attention(lib, qsl=[0, 0], seq=[7]) == 0
+    assert call_attention(lib, qsl=[0], seq=[], R=0, stride=1) == 0
+
+
+def test_write_kv_validation(lib):
+    st = lib.cb_write_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 16, 1, 60, 1, None, None)
+    assert st == 3  # 1 * 60 * 2 bytes is not a multiple of 16
+    st = lib.cb_write_kv(None, FAKE, FAKE, FAKE, FAKE, 4, 10, 16, 2, 64, 1, None, None)
+    assert st == 1
+    st = lib.cb_write_kv(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 4, 10, 16, 2, 64, 1, None, None)
+    assert st == 1
+    assert lib.cb_write_kv(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, 16, 2, 64, 1, None, None) == 0
+
+
+def test_binding_raises_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(cb, "_LIB", None)
+    monkeypatch.setenv("CB_LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        cb.lib()

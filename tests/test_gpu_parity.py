@@ -1,0 +1,190 @@
+"""GPU parity: the C-ABI path on cuda:0 against the CPU oracle on the same seeded inputs.
+
+Scatter: bit-exact on the whole pool except the reserved pages 0-1.
+Attention: bf16 within max-abs 2e-2 and mean-abs 2e-3; fp32 within max-abs 1e-4.
+Full-size steps are checked on sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_cb_gb300 as cb
+import workloads
+from stepcheck import (GpuStep, cache_bits, compare, oracle_cache_bits, oracle_step, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"fast": 0, "portable": cb.CB_FLAG_PORTABLE_ONLY}
+
+
+def full_check(spec, flags=0, scale=None, max_abs=None, mean_abs=None):
+    st = GpuStep(spec)
+    h = st.host_inputs()
+    k_before = st.x["k_cache"].clone()
+    out = st.run(flags=flags, scale=scale)
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) == 0
+    ref = oracle_step(spec, h, scale=scale)
+    mx, mn = compare(spec, out, ref, max_abs=max_abs, mean_abs=mean_abs)
+    # scatter bit-exact outside the reserved pages
+    want = oracle_cache_bits(spec, k_before, st.x["k_new"], spec.slot_mapping)
+    got = cache_bits(st.x["k_cache"])
+    assert np.array_equal(got[2:], want[2:])
+    return mx, mn
+
+
+# ------------------------------------------------------------------ tiny fp32 step
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_tiny_mixed_fp32(path):
+    full_check(workloads.tiny_mixed(), flags=PATHS[path])
+
+
+# ------------------------------------------------------------------ randomised small cases
+
+SMALL = []
+for q_len in (1, 2, 17, 128, 129):
+    for ctx in (0, 1, 15, 16, 17, 1000):
+        SMALL.append((q_len, ctx))
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("BS", [2, 16])
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_small_ragged_bf16(G, BS, path):
+    # all (q_len, ctx) combinations as one ragged step, plus an empty request
+    q_lens = [q for q, _ in SMALL] + [0]
+    ctx = [c for _, c in SMALL] + [5]
+    Hkv = 2
+    spec = workloads.custom(q_lens, ctx, num_q_heads=G * Hkv, num_kv_heads=Hkv, head_dim=128,
+                            block_size=BS, seed=100 + G * 10 + BS)
+    full_check(spec, flags=PATHS[path])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_head_dims_and_dtypes(D, dtype):
+    spec = workloads.custom([1, 5, 1, 33], [40, 0, 7, 100], num_q_heads=8, num_kv_heads=2,
+                            head_dim=D, block_size=16, dtype=dtype, seed=7 + D)
+    full_check(spec)
+
+
+@pytest.mark.parametrize("window", [1, 7, 16, 100])
+def test_sliding_window(window):
+    spec = workloads.custom([1, 20, 1, 64], [300, 50, 16, 0], num_q_heads=16, num_kv_heads=4,
+                            block_size=16, seed=window, sliding_window=window)
+    full_check(spec)
+
+
+def test_sharp_softmax():
+    """Scale x8 makes the softmax peaked so the tolerance bites on the largest weights."""
+    spec = workloads.custom([1, 1, 40, 1], [500, 33, 64, 2000], num_q_heads=32, num_kv_heads=8,
+                            seed=9)
+    full_check(spec, scale=8.0 / np.sqrt(128.0))
+
+
+# ------------------------------------------------------------------ full-size steps
+
+
+def sampled_check(spec, n_rows=64, flags=0):
+    st = GpuStep(spec)
+    h = st.host_inputs()
+    out = st.run(flags=flags)
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) == 0
+    rows = sample_rows(spec, n_rows)
+    ref = oracle_step(spec, h, rows=rows)
+    return compare(spec, out, ref, rows=rows)
+
+
+def test_decode_64_full_size():
+    sampled_check(workloads.decode_step(), n_rows=64)
+
+
+def test_mixed_2048_full_size():
+    sampled_check(workloads.mixed_step(), n_rows=48)
+
+
+@pytest.mark.parametrize("window", [0, 4096])
+def test_long_decode_full_size(window):
+    sampled_check(workloads.long_decode(window=window), n_rows=16)
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+
+def test_physical_page_permutation_is_bitwise_invariant():
+    spec = workloads.custom([1, 9, 1, 30], [77, 0, 500, 40], num_q_heads=32, num_kv_heads=8,
+                            seed=3)
+    st = GpuStep(spec)
+    out1 = st.run(scatter=True).clone()
+    # relabel pages: new_cache[perm[p]] = cache[p]; tables and slots follow
+    rng = np.random.default_rng(1)
+    nb = spec.num_blocks
+    perm = np.arange(nb)
+    perm[2:] = 2 + rng.permutation(nb - 2)
+    pt = torch.from_numpy(perm).cuda()
+    st2 = GpuStep(spec)
+    kc = torch.empty_like(st2.x["k_cache"])
+    vc = torch.empty_like(st2.x["v_cache"])
+    kc[pt] = st2.x["k_cache"]
+    vc[pt] = st2.x["v_cache"]
+    st2.x["k_cache"], st2.x["v_cache"] = kc, vc
+    bt = perm[spec.block_table].astype(np.int32)
+    slots = perm[spec.slot_mapping // spec.block_size] * spec.block_size \
+        + spec.slot_mapping % spec.block_size
+    st2.md["block_table"] = torch.from_numpy(bt).cuda()
+    st2.md["slot_mapping"] = torch.from_numpy(slots).cuda()
+    out2 = st2.run(scatter=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_request_alone_equals_request_in_batch():
+    spec = workloads.custom([1, 37, 1], [900, 300, 64], num_q_heads=32, num_kv_heads=8, seed=4)
+    st = GpuStep(spec)
+    out = st.run()
+    # request 1 alone, same pages and values
+    r = 1
+    t0, t1 = int(spec.query_start_loc[r]), int(spec.query_start_loc[r + 1])
+    alone = workloads.StepSpec(**{**spec.__dict__})
+    alone.q_lens = spec.q_lens[r:r + 1]
+    alone.ctx_lens = spec.ctx_lens[r:r + 1]
+    alone.query_start_loc = np.array([0, t1 - t0], np.int32)
+    alone.seq_lens = spec.seq_lens[r:r + 1]
+    alone.block_table = spec.block_table[r:r + 1]
+    alone.slot_mapping = spec.slot_mapping[t0:t1]
+    st2 = GpuStep(alone)
+    st2.x["k_cache"].copy_(st.x["k_cache"])  # already holds the scattered tokens
+    st2.x["v_cache"].copy_(st.x["v_cache"])
+    st2.x["q"] = st.x["q"][t0:t1].contiguous()
+    out2 = st2.run(scatter=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out[t0:t1], out2)
+
+
+def test_out_of_range_block_id_is_recorded_not_faulted():
+    spec = workloads.custom([1, 3], [40, 10], num_q_heads=8, num_kv_heads=2, seed=5)
+    st = GpuStep(spec)
+    bt = spec.block_table.copy()
+    bt[0, 1] = spec.num_blocks + 5  # past the pool
+    st.md["block_table"] = torch.from_numpy(bt).cuda()
+    st.run(scatter=False)
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) & 0x1
+    assert cb.read_error_word(st.ws) == 0  # cleared by the read
+
+
+def test_out_of_range_slot_is_recorded_and_skipped():
+    spec = workloads.custom([2], [3], num_q_heads=8, num_kv_heads=2, seed=6)
+    st = GpuStep(spec)
+    slots = spec.slot_mapping.copy()
+    slots[0] = spec.num_blocks * spec.block_size + 3
+    slots[1] = -1
+    before = st.x["k_cache"].clone()
+    cb.write_kv(st.x["k_new"], st.x["v_new"], st.x["k_cache"], st.x["v_cache"],
+                torch.from_numpy(slots).cuda(), error_word=st.ws.view(torch.int32)[:1])
+    torch.cuda.synchronize()
+    assert torch.equal(before, st.x["k_cache"])
+    assert cb.read_error_word(st.ws) & 0x2
