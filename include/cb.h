@@ -68,6 +68,7 @@ typedef enum cb_dtype { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
 /* Error-word codes recorded on the device (bit set). */
 #define CB_DEVERR_BLOCK_ID 0x1 /* a block_table entry outside [0, num_blocks) */
 #define CB_DEVERR_SLOT 0x2     /* a slot_mapping entry >= num_blocks * block_size */
+#define CB_DEVERR_TIMEOUT 0x4  /* a pipeline wait gave up (the kernel returned early) */
 
 /* Static string for a status code; never NULL. */
 const char* cb_status_string(int status);
@@ -106,15 +107,17 @@ cb_status cb_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
 /*
  * cb_workspace_size -- bytes of device workspace cb_paged_attention needs for
  * a step with these sizes (an upper bound; it does not depend on the lengths).
- * The workspace holds the device error word and the split-KV partial results.
+ * The workspace holds the device error word, per-request arrival counters and
+ * the split-KV partial results.
  */
 size_t cb_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim);
 
 /*
- * cb_workspace_init -- zero the workspace's error word (asynchronously on
- * `stream`). Call once after allocating a workspace; cb_read_error_word clears
- * it again after each read.
+ * cb_workspace_init -- zero the whole workspace (asynchronously on `stream`).
+ * Call once after allocating a workspace, and again after a call recorded
+ * CB_DEVERR_TIMEOUT. Between calls the library leaves the workspace's
+ * counters at zero itself; cb_read_error_word clears the error word.
  */
 cb_status cb_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 

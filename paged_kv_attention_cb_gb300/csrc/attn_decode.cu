@@ -1,0 +1,778 @@
+// Decode rows (q_len == 1) of the step: split-KV paged attention, bf16.
+//
+// What it computes is the decode case of the per-block pseudocode of
+// "Continuous Batching" (languisher.top), section "Extension: the vLLM v1
+// implementation": context_len = seq_len - 1, the single query attends
+// kv_pos 0 .. context_len (or the last sliding_window positions), each
+// resolved through block_table[req][kv_pos / BLOCK_SIZE] at offset
+// kv_pos % BLOCK_SIZE. Decode is memory-bound ("Continuous batching
+// mechanics", d9bl.com, section "A single request on a GPU"), so the design
+// goal is to stream every attended K/V byte from HBM exactly once at full
+// bandwidth:
+//
+// * Work partition. The decode requests' key blocks (16 keys of one request,
+//   all KV heads) are numbered in request order, u = 0 .. U-1, and CTA b of C
+//   takes the contiguous range [b*U/C, (b+1)*U/C): every CTA streams the same
+//   number of bytes whatever the length mix, and a long request is split
+//   across CTAs (split-KV). Each CTA finds its first request with a block scan
+//   over the decode lengths, then walks forward. A piece of a request inside
+//   one CTA is a segment; a request that lies in one CTA writes its output
+//   directly, otherwise each segment writes an unnormalised partial
+//   (m, l, o) and a bookkeeping warp bumps the request's arrival counter off
+//   the streaming path; the CTA that delivers the last partial merges them
+//   (log-sum-exp) after its own stream and resets the counter, so no second
+//   kernel is needed.
+// * GQA packing. One CTA covers up to 8 KV heads (one consumer warp each) and
+//   all G query heads of each KV head, so K/V are read once for the group.
+// * Staging. A producer warp moves each 16-key block of all the CTA's heads
+//   with four 128B-swizzled TMA tile loads (K and V, two 64-element halves of
+//   D) into a STAGES-deep ring of shared-memory buffers guarded by mbarriers;
+//   the request's query rows arrive by a 1-D bulk copy into a 2-slot ring.
+// * Contraction. Per warp and block: S^T (16 keys x 8 heads) = K Q^T and
+//   O^T (D x 8 heads) += V^T P^T on mma.sync m16n8k16 (bf16 in, fp32
+//   accumulate); the key axis is the M dimension so a group of G <= 8 query
+//   heads fills the N = 8 columns. P^T goes from the accumulator layout to the
+//   B-operand layout with movmatrix. Softmax statistics are per column, kept
+//   per lane and reduced with warp shuffles.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <float.h>
+
+#include "common.cuh"
+#include "decode.h"
+#include "launch.h"
+#include "sm100_ptx.cuh"
+
+namespace cb {
+
+namespace {
+
+constexpr int kKB = 16;  // keys per block (stage)
+
+struct SegDesc {
+  int r;       // request (-1: no more segments)
+  int kb0;     // first key block (absolute, within the request)
+  int kb1;     // one past the last key block
+  int t;       // packed query row of the request
+  int lo;      // first attended key (window start)
+  int hi;      // last attended key (= seq_len - 1)
+  int slot;    // partial slot (r + CTA index)
+  int direct;  // 1: the request lies wholly in this CTA
+  int b_first; // first CTA of the request
+  int nseg;    // number of CTAs (segments) of the request
+};
+
+constexpr int kDoneRing = 4;  // split segments handed to the bookkeeping warp (<= 2) + end mark
+
+struct DecodeSmem {
+  uint64_t full[kDecodeMaxStages];
+  uint64_t empty[kDecodeMaxStages];
+  uint64_t qfull[2];
+  uint64_t qempty[2];
+  uint64_t done_full[kDoneRing];
+  uint64_t merges_ready;
+  SegDesc seg[2];
+  SegDesc done[kDoneRing];
+  long long scan[16];
+  int pend[kDoneRing];
+  int npend;
+  int first_r;
+  long long first_u;
+  int abort_flag;
+};
+
+CB_DEV int kb_lo_of(int seq, int window) {
+  const int lo = window > 0 ? max(0, seq - window) : 0;
+  return lo / kKB;
+}
+
+// Key blocks of request r if it is a decode request, else 0.
+CB_DEV int decode_units(const DecodeArgs& p, int r, int* seq_out, int* t_out) {
+  const int q0 = __ldg(p.a.query_start_loc + r);
+  const int q1 = __ldg(p.a.query_start_loc + r + 1);
+  if (q1 - q0 != 1) return 0;
+  const int seq = __ldg(p.a.seq_lens + r);
+  if (seq <= 0) return 0;
+  *seq_out = seq;
+  *t_out = q0;
+  return (seq - 1) / kKB - kb_lo_of(seq, p.a.sliding_window) + 1;
+}
+
+// CTA that owns global key block u (ranges [b*U/C, (b+1)*U/C)).
+CB_DEV int cta_of(long long u, long long U, int C) {
+  return (int)(((u + 1) * (long long)C + U - 1) / U) - 1;
+}
+
+CB_DEV float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+CB_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+CB_DEV long long warp_incl_scan(long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += n;
+  }
+  return v;
+}
+
+// Log-sum-exp merge of the nseg partials of request d.r for this warp's G
+// query heads: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s. With at
+// most 32 segments the statistics take one batch of loads (lane s holds
+// segment s) and the partial outputs are loaded several segments at a time,
+// so a merge costs a couple of L2 round trips.
+template <int D, int G>
+CB_DEV void merge_partials(const DecodeArgs& p, const SegDesc& d, int qh_base, int q_row_elems) {
+  constexpr int J = G * D / 32;        // output elements per lane
+  constexpr int SB = G <= 4 ? 4 : 2;   // segments loaded per batch
+  const int lane = threadIdx.x & 31;
+  const int Hq = p.a.num_q_heads;
+  const int nseg = d.nseg;
+  const long long slot0 = (long long)d.r + d.b_first;
+  float acc[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) acc[j] = 0.f;
+  float M[G], L[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) M[h] = -FLT_MAX;
+  // running maximum over all segments (lane-parallel, 32 segments per pass)
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    if (s0 + lane < nseg) {
+      const float2* ml = p.part_ml + (slot0 + s0 + lane) * Hq + qh_base;
+#pragma unroll
+      for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&ml[h].x));
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    M[h] = warp_max(M[h]);
+    L[h] = 0.f;
+  }
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    // weights of segments s0 + lane
+    float w[G];
+    if (s0 + lane < nseg) {
+      const float2* ml = p.part_ml + (slot0 + s0 + lane) * Hq + qh_base;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float2 v = __ldcg(&ml[h]);
+        w[h] = exp2f(v.x - M[h]);
+        L[h] += w[h] * v.y;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) w[h] = 0.f;
+    }
+    const int n = min(32, nseg - s0);
+    for (int k = 0; k < n; k += SB) {
+      float v[SB][J];
+#pragma unroll
+      for (int sb = 0; sb < SB; ++sb) {
+        const float* o = p.part_o + ((slot0 + s0 + k + sb) * Hq + qh_base) * D;
+#pragma unroll
+        for (int j = 0; j < J; ++j) v[sb][j] = k + sb < n ? __ldcg(o + j * 32 + lane) : 0.f;
+      }
+#pragma unroll
+      for (int sb = 0; sb < SB; ++sb) {
+        const int src = min(k + sb, 31);
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const float ws = __shfl_sync(0xffffffffu, w[(j * 32) / D], src);
+          acc[j] = fmaf(ws, v[sb][j], acc[j]);
+        }
+      }
+    }
+  }
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems +
+                       qh_base * D;
+#pragma unroll
+  for (int h = 0; h < G; ++h) L[h] = 1.f / warp_sum(L[h]);
+#pragma unroll
+  for (int j = 0; j < J; ++j) out[j * 32 + lane] = __float2bfloat16_rn(acc[j] * L[(j * 32) / D]);
+}
+
+}  // namespace
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecodeMaxHeads * 32 + 64, 1)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs p) {
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(G >= 1 && G <= 8, "group");
+  constexpr int kHalves = D / 64;
+  constexpr int kKSteps = D / 16;
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const int HB = p.heads_per_cta;
+  const int box_bytes = HB * kKB * 128;  // one 64-element half of D, all heads, 16 keys
+  uint8_t* stages = base;
+  uint8_t* qring = base + p.stages * p.stage_bytes;
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(qring + 2 * p.q_slot_bytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nthreads = blockDim.x;
+  const int b = blockIdx.x;
+  const int hg = blockIdx.y;
+  const int C = p.num_ctas;
+  const long long U = p.total_units;
+  const int R = p.a.num_requests;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], HB);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.qfull[s], 1);
+      mbar_init(&sm.qempty[s], HB);
+    }
+    for (int s = 0; s < kDoneRing; ++s) mbar_init(&sm.done_full[s], HB * 32);
+    mbar_init(&sm.merges_ready, 1);
+    sm.first_r = -1;
+    sm.first_u = 0;
+    sm.abort_flag = 0;
+    sm.npend = 0;
+    fence_barrier_init();
+  }
+  if (warp == HB && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  // The metadata (and q) were written before the step's first kernel: when
+  // that kernel is libcb's own scatter, which lets this grid start only after
+  // its own wait on the previous grid, they are visible already and only the
+  // cache reads (the producer's TMA) must wait for the scatter. Otherwise this
+  // is the step's first kernel and every thread waits.
+  if (!p.metadata_ready) grid_dependency_wait();
+  __syncthreads();
+
+  const long long u_lo = (long long)b * U / C;
+  const long long u_hi = (long long)(b + 1) * U / C;
+
+  // ---- this CTA's first request: from the host's table, or by a block scan
+  if (p.has_table) {
+    if (threadIdx.x == 0) {
+      sm.first_r = p.cta_first[b].x;
+      sm.first_u = p.cta_first[b].y;
+    }
+    __syncthreads();
+  } else if (u_lo < u_hi) {
+    long long carry = 0;
+    for (int base_r = 0; base_r < R; base_r += nthreads) {
+      const int r = base_r + threadIdx.x;
+      int seq = 0, t = 0, units = 0;
+      if (r < R) units = decode_units(p, r, &seq, &t);
+      long long v = warp_incl_scan(units);
+      if (lane == 31) sm.scan[warp] = v;
+      __syncthreads();
+      if (warp == 0) {
+        long long w = lane < (nthreads >> 5) ? sm.scan[lane] : 0;
+        w = warp_incl_scan(w);
+        if (lane < (nthreads >> 5)) sm.scan[lane] = w;  // inclusive totals per warp
+      }
+      __syncthreads();
+      const long long before = carry + (warp > 0 ? sm.scan[warp - 1] : 0);
+      const long long incl = before + v;
+      const long long excl = incl - units;
+      if (units > 0 && excl <= u_lo && u_lo < incl) {
+        sm.first_r = r;
+        sm.first_u = excl;
+      }
+      carry += sm.scan[(nthreads >> 5) - 1];
+      __syncthreads();
+      if (sm.first_r >= 0) break;
+    }
+  }
+  allow_dependent_launch();
+
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.a.q);
+  const int q_row_elems = p.a.num_q_heads * D;
+  const uint32_t q_bytes = (uint32_t)(HB * G * D * 2);
+
+  if (warp == HB) {
+    // =================================================== producer warp
+    // Request metadata is read 32 requests at a time (lane l holds request
+    // wbase + l), and the block-table entries of the next batch of 32 key
+    // blocks are requested one batch ahead, so segment switches do not stall
+    // the TMA issue on global-memory latency.
+    int k = 0;        // segments published
+    long long i = 0;  // stages issued
+    bool ok = true;
+    int wbase = -1, w_units = 0, w_seq = 0, w_t = 0;
+    auto load_window = [&](int r0) {
+      wbase = r0;
+      const int r = r0 + lane;
+      int seq = 0, t = 0, units = 0;
+      if (r < R) units = decode_units(p, r, &seq, &t);
+      w_units = units;
+      w_seq = seq;
+      w_t = t;
+    };
+    // next decode request at or after r (R when none)
+    auto next_decode = [&](int r) -> int {
+      while (r < R) {
+        if (r - wbase >= 32 || r < wbase) load_window(r);
+        const unsigned m = __ballot_sync(0xffffffffu, w_units > 0 && wbase + lane >= r);
+        if (m) return wbase + __ffs(m) - 1;
+        r = wbase + 32;
+      }
+      return R;
+    };
+    auto load_pages = [&](int r, int kb_start, int n) -> int {
+      int pg = 0;
+      if (lane < n)
+        pg = __ldg(p.a.block_table + (long long)r * p.a.bt_stride +
+                   (kb_start + lane) * kKB / p.a.block_size);
+      return pg;
+    };
+    // walk state of the current segment
+    int r = -1, seq = 0, t = 0, units = 0;
+    long long u_r = 0, u = u_lo;
+    if (u_lo < u_hi && sm.first_r >= 0) {
+      r = sm.first_r;
+      u_r = sm.first_u;
+      load_window(r);
+    }
+    auto fetch = [&](int rr) {
+      const int j = rr - wbase;
+      units = __shfl_sync(0xffffffffu, w_units, j);
+      seq = __shfl_sync(0xffffffffu, w_seq, j);
+      t = __shfl_sync(0xffffffffu, w_t, j);
+    };
+    int kb0 = 0, kb1 = 0;
+    int pages = 0;  // page ids of the batch about to be issued (lane j: key block kb + j)
+    if (r >= 0) {
+      fetch(r);
+      const int kbl = kb_lo_of(seq, p.a.sliding_window);
+      kb0 = kbl + (int)(u - u_r);
+      kb1 = kbl + (int)(min(u_r + units, u_hi) - u_r);
+      pages = load_pages(r, kb0, min(32, kb1 - kb0));
+    }
+    if (p.metadata_ready) grid_dependency_wait();  // the scatter must be complete
+    while (r >= 0 && ok) {
+      const long long seg_u1 = min(u_r + units, u_hi);
+      const int b_first = cta_of(u_r, U, C);
+      const int b_last = cta_of(u_r + units - 1, U, C);
+      const int qs = k & 1;
+      if (k >= 2 && !mbar_wait(&sm.qempty[qs], ((k >> 1) - 1) & 1)) { ok = false; break; }
+      if (lane == 0) {
+        SegDesc& d = sm.seg[qs];
+        d.r = r;
+        d.kb0 = kb0;
+        d.kb1 = kb1;
+        d.t = t;
+        d.lo = p.a.sliding_window > 0 ? max(0, seq - p.a.sliding_window) : 0;
+        d.hi = seq - 1;
+        d.slot = r + b;
+        d.direct = (b_first == b_last);
+        d.b_first = b_first;
+        d.nseg = b_last - b_first + 1;
+        mbar_arrive_expect_tx(&sm.qfull[qs], q_bytes);
+        bulk_load(qring + qs * p.q_slot_bytes,
+                  q + (long long)t * q_row_elems + (long long)hg * HB * G * D, q_bytes,
+                  &sm.qfull[qs]);
+      }
+      __syncwarp();
+      // the segment after this one (to prefetch its first page ids)
+      int nr = -1, nkb0 = 0, nkb1 = 0;
+      long long nu_r = u_r + units;
+      if (seg_u1 < u_hi) {
+        nr = next_decode(r + 1);
+        if (nr >= R) nr = -1;
+      }
+      for (int kb_base = kb0; kb_base < kb1 && ok; kb_base += 32) {
+        const int nkb = min(32, kb1 - kb_base);
+        const int cur = pages;
+        // the batch after this one: rest of this segment, or the next segment's start
+        if (kb_base + 32 < kb1) {
+          pages = load_pages(r, kb_base + 32, min(32, kb1 - kb_base - 32));
+        } else if (nr >= 0) {
+          const int j = nr - wbase;
+          const int n_units = __shfl_sync(0xffffffffu, w_units, j);
+          const int n_seq = __shfl_sync(0xffffffffu, w_seq, j);
+          const int nkbl = kb_lo_of(n_seq, p.a.sliding_window);
+          nkb0 = nkbl;
+          nkb1 = nkbl + (int)(min(nu_r + n_units, u_hi) - nu_r);
+          pages = load_pages(nr, nkb0, min(32, nkb1 - nkb0));
+        }
+        for (int j = 0; j < nkb; ++j) {
+          const int pg = __shfl_sync(0xffffffffu, cur, j);
+          const int kb = kb_base + j;
+          const int s = (int)(i % p.stages);
+          if (i >= p.stages && !mbar_wait(&sm.empty[s], (uint32_t)(((i / p.stages) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) { ok = false; break; }
+          if (lane == 0) {
+            int pgc = pg;
+            if (pg < 0 || pg >= p.a.num_blocks) {
+              record_error(p.a.error_word, CB_DEVERR_BLOCK_ID_CODE);
+              pgc = p.a.num_blocks;  // TMA reads past the pool as zeros
+            }
+            const int key0 = (kb * kKB) % p.a.block_size;
+            uint8_t* st = stages + s * p.stage_bytes;
+            mbar_arrive_expect_tx(&sm.full[s], (uint32_t)p.stage_bytes);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h) {
+              tma_load_4d(st + h * box_bytes, &tmap_k, &sm.full[s], h * 64, key0, hg * HB, pgc);
+              tma_load_4d(st + (kHalves + h) * box_bytes, &tmap_v, &sm.full[s], h * 64, key0,
+                          hg * HB, pgc);
+            }
+          }
+          __syncwarp();
+          ++i;
+        }
+      }
+      ++k;
+      if (nr < 0) break;
+      // advance to the next segment
+      r = nr;
+      u_r = nu_r;
+      u = seg_u1;
+      fetch(r);
+      kb0 = nkb0;
+      kb1 = nkb1;
+    }
+    if (ok) {
+      // terminator
+      const int qs = k & 1;
+      if (k >= 2 && !mbar_wait(&sm.qempty[qs], ((k >> 1) - 1) & 1)) ok = false;
+      if (ok && lane == 0) {
+        sm.seg[qs].r = -1;
+        mbar_arrive(&sm.qfull[qs]);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+        sm.abort_flag = 1;
+        // drain the copies this warp issued before leaving
+        const long long first = i > p.stages ? i - p.stages : 0;
+        for (long long j = first; j < i; ++j)
+          mbar_wait(&sm.full[j % p.stages], (uint32_t)((j / p.stages) & 1));
+      }
+    }
+    return;
+  }
+
+  if (warp == HB + 1) {
+    // =================================================== arrival bookkeeping
+    // For every segment whose request spans several CTAs: make its partials
+    // visible device-wide, count its arrival, and remember the requests whose
+    // last partial this CTA delivered (merged by the consumers at the end).
+    int nd = 0, npend = 0;
+    for (;; ++nd) {
+      if (nd >= kDoneRing || !mbar_wait(&sm.done_full[nd], 0)) {
+        if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
+        break;
+      }
+      const SegDesc dd = sm.done[nd];
+      if (dd.r < 0) break;
+      __threadfence();
+      int last = 0;
+      if (lane == 0) {
+        int* cnt = p.counters + (long long)dd.r * gridDim.y + hg;
+        const int old = atomicAdd(cnt, 1);
+        last = old == dd.nseg - 1;
+        if (last) *cnt = 0;  // every segment has arrived: ready for the next step
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        if (lane == 0) sm.pend[npend] = nd;
+        ++npend;
+      }
+    }
+    __threadfence();
+    if (lane == 0) {
+      sm.npend = npend;
+      mbar_arrive(&sm.merges_ready);
+    }
+    return;
+  }
+
+  // ===================================================== consumer warps
+  const int hl = warp;  // local KV head
+  const int gid = lane >> 2;
+  const int tq = lane & 3;
+  const float sl2 = p.a.scale_log2;
+  int nd = 0;  // segments handed to the bookkeeping warp
+  long long i = 0;
+  for (int k = 0;; ++k) {
+    const int qs = k & 1;
+    if (!mbar_wait(&sm.qfull[qs], (k >> 1) & 1)) {
+      if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
+      return;
+    }
+    const SegDesc d = sm.seg[qs];
+    if (d.r < 0) break;
+    // query fragments (B operand of S^T = K Q^T): Q[head = gid][d = 16ks + 2tq (+8)]
+    uint32_t qf[kKSteps][2];
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qring + qs * p.q_slot_bytes +
+                                                               (hl * G + gid) * D * 2);
+#pragma unroll
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        qf[ks][0] = gid < G ? qrow[(16 * ks + 2 * tq) >> 1] : 0u;
+        qf[ks][1] = gid < G ? qrow[(16 * ks + 2 * tq + 8) >> 1] : 0u;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.qempty[qs]);
+
+    float o[kKSteps][4];
+#pragma unroll
+    for (int m = 0; m < kKSteps; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+    float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
+
+    for (int kb = d.kb0; kb < d.kb1; ++kb, ++i) {
+      const int s = (int)(i % p.stages);
+      if (!mbar_wait(&sm.full[s], (uint32_t)((i / p.stages) & 1))) {
+        if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
+        return;
+      }
+      const uint8_t* ks_base = stages + s * p.stage_bytes;
+      uint8_t* vs_base = stages + s * p.stage_bytes + kHalves * box_bytes;
+      const int key_base = kb * kKB;
+      // zero V rows past the last attended key (their page slots hold unrelated data)
+      if (key_base + kKB - 1 > d.hi) {
+        const int first_bad = d.hi - key_base + 1;
+        const int nbad = kKB - first_bad;
+        for (int e = lane; e < nbad * kHalves * 8; e += 32) {
+          const int row = first_bad + e / (kHalves * 8);
+          const int rem = e % (kHalves * 8);
+          const int h = rem >> 3;
+          const int c = rem & 7;
+          *reinterpret_cast<uint4*>(vs_base + h * box_bytes + (hl * kKB + row) * 128 + c * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // ---- S^T = K Q^T  (16 keys x 8 heads)
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int jm = lane >> 3;
+        const int key = (lane & 7) + ((jm & 1) << 3);
+        const uint32_t row_addr = smem_u32(ks_base) + (hl * kKB + key) * 128;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+          const int chunk = (ks & 3) * 2 + (jm >> 1);
+          uint32_t a[4];
+          ldmatrix_x4(a, row_addr + (ks >> 2) * box_bytes + ((chunk ^ (key & 7)) << 4));
+          mma_bf16_16816(sacc, a, qf[ks][0], qf[ks][1]);
+        }
+      }
+      // ---- mask, online softmax per head column (2tq, 2tq+1)
+      const int k0 = key_base + gid;
+      const int k1 = k0 + 8;
+      const bool v0 = k0 >= d.lo && k0 <= d.hi;
+      const bool v1 = k1 >= d.lo && k1 <= d.hi;
+      const float s0 = v0 ? sacc[0] * sl2 : -INFINITY;
+      const float s1 = v0 ? sacc[1] * sl2 : -INFINITY;
+      const float s2 = v1 ? sacc[2] * sl2 : -INFINITY;
+      const float s3 = v1 ? sacc[3] * sl2 : -INFINITY;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 = l0 * a0 + (p0 + p2);
+      l1 = l1 * a1 + (p1 + p3);
+#pragma unroll
+      for (int m = 0; m < kKSteps; ++m) {
+        o[m][0] *= a0;
+        o[m][1] *= a1;
+        o[m][2] *= a0;
+        o[m][3] *= a1;
+      }
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
+      // ---- O^T += V^T P^T  (D x 8 heads)
+      {
+        const int jm = lane >> 3;
+        const int key = (lane & 7) + ((jm >> 1) << 3);
+        const uint32_t row_addr = smem_u32(vs_base) + (hl * kKB + key) * 128;
+#pragma unroll
+        for (int m = 0; m < kKSteps; ++m) {
+          const int chunk = 2 * m + (jm & 1);
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, row_addr + (chunk >> 3) * box_bytes +
+                                   (((chunk & 7) ^ (key & 7)) << 4));
+          mma_bf16_16816(o[m], a, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+    }
+
+    // ---- segment epilogue
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;
+    const int qh_base = (hg * HB + hl) * G;
+    if (d.direct) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems;
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+      for (int m = 0; m < kKSteps; ++m) {
+        const int dd = 16 * m + gid;
+        if (h0 < G) {
+          out[(qh_base + h0) * D + dd] = __float2bfloat16_rn(o[m][0] * i0);
+          out[(qh_base + h0) * D + dd + 8] = __float2bfloat16_rn(o[m][2] * i0);
+        }
+        if (h1 < G) {
+          out[(qh_base + h1) * D + dd] = __float2bfloat16_rn(o[m][1] * i1);
+          out[(qh_base + h1) * D + dd + 8] = __float2bfloat16_rn(o[m][3] * i1);
+        }
+      }
+    } else {
+      float* po = p.part_o + (long long)d.slot * q_row_elems;
+#pragma unroll
+      for (int m = 0; m < kKSteps; ++m) {
+        const int dd = 16 * m + gid;
+        if (h0 < G) {
+          po[(qh_base + h0) * D + dd] = o[m][0];
+          po[(qh_base + h0) * D + dd + 8] = o[m][2];
+        }
+        if (h1 < G) {
+          po[(qh_base + h1) * D + dd] = o[m][1];
+          po[(qh_base + h1) * D + dd + 8] = o[m][3];
+        }
+      }
+      if (gid == 0) {
+        float2* pml = p.part_ml + (long long)d.slot * p.a.num_q_heads;
+        if (h0 < G) pml[qh_base + h0] = make_float2(m0, l0);
+        if (h1 < G) pml[qh_base + h1] = make_float2(m1, l1);
+      }
+      // hand the segment to the bookkeeping warp (at most two per CTA: only
+      // a CTA's first and last segments can belong to a split request)
+      if (nd < kDoneRing - 1) {
+        if (hl == 0 && lane == 0) sm.done[nd] = d;
+        mbar_arrive(&sm.done_full[nd]);
+      } else if (lane == 0) {
+        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+      }
+      ++nd;
+    }
+  }
+  // ---- end of the stream: close the hand-off ring, then merge the requests
+  // whose last partial this CTA delivered
+  if (nd < kDoneRing) {
+    if (hl == 0 && lane == 0) sm.done[nd].r = -1;
+    mbar_arrive(&sm.done_full[nd]);
+  }
+  if (!mbar_wait(&sm.merges_ready, 0)) {
+    if (lane == 0) record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+    return;
+  }
+  const int npend = *reinterpret_cast<volatile int*>(&sm.npend);
+  for (int j = 0; j < npend; ++j) {
+    const SegDesc d = sm.done[sm.pend[j]];
+    __threadfence();
+    merge_partials<D, G>(p, d, (hg * HB + hl) * G, q_row_elems);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 4-D view of a cache [NB, BS, Hkv, D] as (d, key-in-page, head, page) so that
+// a box (64, 16, HB, 1) lands in shared memory head-major: rows (head, key).
+cudaError_t make_cache_map(CUtensorMap* map, void* cache, const StepArgs& a, int hb) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t elt = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)a.head_dim, (cuuint64_t)a.block_size,
+                        (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)a.num_kv_heads * a.head_dim * elt,
+                           (cuuint64_t)a.head_dim * elt,
+                           (cuuint64_t)a.block_size * a.num_kv_heads * a.head_dim * elt};
+  cuuint32_t box[4] = {64, 16, (cuuint32_t)hb, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                      size_t smem, int hg, int num_requests, cudaStream_t s) {
+  auto kern = decode_split_kernel<D, G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDecodeSmemLimit);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  (void)num_requests;
+  return launch_pdl(kDecodeSplit, kern, dim3(p.num_ctas, hg), dim3(p.heads_per_cta * 32 + 64),
+                    smem, s, mk, mv, p);
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                     size_t smem, int hg, int R, cudaStream_t s) {
+  switch (p.a.num_q_heads / p.a.num_kv_heads) {
+    case 1: return launch_dg<D, 1>(p, mk, mv, smem, hg, R, s);
+    case 2: return launch_dg<D, 2>(p, mk, mv, smem, hg, R, s);
+    case 4: return launch_dg<D, 4>(p, mk, mv, smem, hg, R, s);
+    case 8: return launch_dg<D, 8>(p, mk, mv, smem, hg, R, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes) {
+  return 1024 /* alignment slack */ + (size_t)stages * stage_bytes + 2 * (size_t)q_slot_bytes +
+         sizeof(DecodeSmem);
+}
+
+cudaError_t launch_decode(DecodeArgs p, const DecodePlan& plan, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  cudaError_t e = make_cache_map(&mk, p.a.k_cache, p.a, p.heads_per_cta);
+  if (e == cudaSuccess) e = make_cache_map(&mv, p.a.v_cache, p.a, p.heads_per_cta);
+  if (e != cudaSuccess) return e;
+  const int hg = p.a.num_kv_heads / p.heads_per_cta;
+  if (p.a.head_dim == 64) return launch_d<64>(p, mk, mv, plan.smem_bytes, hg, p.a.num_requests, stream);
+  return launch_d<128>(p, mk, mv, plan.smem_bytes, hg, p.a.num_requests, stream);
+}
+
+}  // namespace cb

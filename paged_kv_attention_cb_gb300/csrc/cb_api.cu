@@ -92,8 +92,7 @@ size_t cb_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_q
 cb_status cb_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < cb::kWorkspaceHeaderBytes)
     return fail(CB_ERR_WORKSPACE, "workspace missing or smaller than its header");
-  cudaError_t e = cudaMemsetAsync(workspace, 0, cb::kWorkspaceHeaderBytes,
-                                  static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "workspace init");
   return CB_OK;
 }
@@ -205,7 +204,8 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
   a.error_word = error_word;
 
   cb::Plan plan;
-  cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, workspace, workspace_bytes);
+  cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, workspace,
+                workspace_bytes);
   cudaError_t e = cb::run_plan(plan, a, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return CB_OK;

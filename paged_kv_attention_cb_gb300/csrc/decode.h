@@ -1,0 +1,40 @@
+// Decode split-KV kernel: arguments shared by the host planner and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace cb {
+
+constexpr int kDecodeMaxStages = 8;
+constexpr int kDecodeMaxHeads = 8;          // KV heads per CTA (one consumer warp each)
+constexpr int kDecodeSmemLimit = 232448;    // 227 KiB dynamic shared memory per CTA
+constexpr int kDecodeTableCtas = 256;       // CTAs whose start is passed in the arguments
+constexpr int CB_DEVERR_BLOCK_ID_CODE = 0x1;
+constexpr int CB_DEVERR_TIMEOUT_CODE = 0x4;
+
+struct DecodeArgs {
+  StepArgs a;
+  long long total_units;  // key blocks of all decode requests
+  int num_ctas;           // C
+  int heads_per_cta;      // HB
+  int stages;
+  int stage_bytes;        // K + V of one 16-key block for HB heads
+  int q_slot_bytes;       // HB * G * D * 2
+  int metadata_ready;     // the step's previous kernel is libcb's scatter
+  float* part_o;          // [slots][Hq][D] unnormalised partial outputs
+  float2* part_ml;        // [slots][Hq] (running max in log2 units, sum)
+  int* counters;          // [R][head groups] arrivals of split requests (zero between steps)
+  int has_table;          // cta_first is filled (num_ctas <= kDecodeTableCtas)
+  int2 cta_first[kDecodeTableCtas];  // per CTA: (first request, its first key-block index)
+};
+
+struct DecodePlan {
+  size_t smem_bytes;
+};
+
+size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes);
+cudaError_t launch_decode(DecodeArgs p, const DecodePlan& plan, cudaStream_t stream);
+
+}  // namespace cb

@@ -31,10 +31,8 @@ enum KernelId {
   kWriteKv = 0,
   kPortableAttention = 1,
   kDecodeSplit = 2,
-  kDecodeCombine = 3,
-  kPrefillTc = 4,
-  kPlan = 5,
-  kNumKernels = 6
+  kPrefillTc = 3,
+  kNumKernels = 4
 };
 
 void note_launch_begin(KernelId id, cudaStream_t stream);

@@ -1,35 +1,132 @@
 // Host-side planning of one step from the host mirrors of the metadata. The
 // scheduler metadata "already divides the work into a request's query tile /
 // KV tile" ("Continuous Batching", languisher.top, section "Extension: the
-// vLLM v1 implementation"); here that division is made per call.
+// vLLM v1 implementation"); here that division is made per call: decode rows
+// go to the split-KV kernel with a byte-balanced partition, prefill rows to
+// the prefill kernel, and whatever the fast kernels do not cover to the
+// portable kernel.
+#include <algorithm>
+
 #include "cb.h"
+#include "decode.h"
 #include "plan.h"
 
 namespace cb {
 
+namespace {
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+struct WorkspaceLayout {
+  size_t counters, part_ml, part_o, total;
+};
+
+WorkspaceLayout layout(int32_t R, int32_t Hq, int32_t Hkv, int32_t D) {
+  WorkspaceLayout w;
+  const size_t slots = (size_t)std::max(R, 0) + kMaxDecodeCtas;
+  const size_t head_groups = (size_t)(std::max(Hkv, 1) + kDecodeMaxHeads - 1) / kDecodeMaxHeads;
+  w.counters = kWorkspaceHeaderBytes;
+  w.part_ml = w.counters + align256((size_t)std::max(R, 1) * head_groups * 4);
+  w.part_o = w.part_ml + align256(slots * Hq * 8);
+  w.total = w.part_o + slots * Hq * (size_t)D * 4;
+  return w;
+}
+
+int decode_units_host(int seq, int window) {
+  const int lo = window > 0 ? std::max(0, seq - window) : 0;
+  return (seq - 1) / 16 - lo / 16 + 1;
+}
+
+}  // namespace
+
 size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim) {
   (void)num_tokens;
-  (void)num_kv_heads;
   if (num_requests < 0 || num_q_heads <= 0 || head_dim <= 0) return kWorkspaceHeaderBytes;
-  const size_t segments = (size_t)num_requests + kMaxDecodeCtas;
-  const size_t partial = (size_t)num_q_heads * (head_dim + 2) * sizeof(float);
-  return kWorkspaceHeaderBytes + segments * partial;
+  return layout(num_requests, num_q_heads, num_kv_heads, head_dim).total;
 }
 
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
-               uint32_t flags, void* workspace, size_t workspace_bytes) {
-  (void)h_qsl;
-  (void)h_seq_lens;
+               uint32_t flags, bool scatter_first, void* workspace, size_t workspace_bytes) {
   plan.workspace = workspace;
   plan.workspace_bytes = workspace_bytes;
   plan.fast_decode = false;
   plan.fast_prefill = false;
   plan.portable_mode = 0;
   if ((flags & CB_FLAG_PORTABLE_ONLY) || a.dtype == CB_F32) return;
+
+  // ---- which rows exist
+  long long U = 0;
+  bool has_prefill = false;
+  for (int r = 0; r < a.num_requests; ++r) {
+    const int ql = h_qsl[r + 1] - h_qsl[r];
+    if (ql == 1 && h_seq_lens[r] > 0) U += decode_units_host(h_seq_lens[r], a.sliding_window);
+    else if (ql > 1) has_prefill = true;
+  }
+
+  // ---- decode rows: split-KV kernel
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
+  const bool decode_ok = U > 0 && a.block_size % 16 == 0 && G <= 8 &&
+                         a.num_kv_heads % HB == 0;
+  if (decode_ok) {
+    DecodeArgs& d = plan.decode;
+    d.a = a;
+    d.heads_per_cta = HB;
+    d.total_units = U;
+    d.num_ctas = (int)std::min<long long>(std::min(sm_count(), kMaxDecodeCtas), U);
+    d.stage_bytes = 2 * (a.head_dim / 64) * HB * 16 * 128;
+    d.q_slot_bytes = HB * G * a.head_dim * 2;
+    const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
+    d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
+    d.metadata_ready = scatter_first ? 1 : 0;
+    // where each CTA's range [b*U/C, (b+1)*U/C) starts: (request, its first unit)
+    d.has_table = d.num_ctas <= kDecodeTableCtas;
+    if (d.has_table) {
+      long long u = 0;
+      int b = 0;
+      const long long C = d.num_ctas;
+      for (int r = 0; r < a.num_requests && b < d.num_ctas; ++r) {
+        const int ql = h_qsl[r + 1] - h_qsl[r];
+        if (ql != 1 || h_seq_lens[r] <= 0) continue;
+        const int units = decode_units_host(h_seq_lens[r], a.sliding_window);
+        while (b < d.num_ctas && (long long)b * U / C < u + units) {
+          d.cta_first[b] = make_int2(r, (int)u);
+          ++b;
+        }
+        u += units;
+      }
+      for (; b < d.num_ctas; ++b) d.cta_first[b] = make_int2(-1, 0);
+    }
+    const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    d.counters = reinterpret_cast<int*>(ws + w.counters);
+    d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+    d.part_o = reinterpret_cast<float*>(ws + w.part_o);
+    plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
+    if (d.stages >= 2) plan.fast_decode = true;
+  }
+  if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
 }
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {
+  if (plan.fast_decode) {
+    cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (plan.portable_mode >= 0) {
     cudaError_t e = launch_portable_attention(a, plan.portable_mode, stream);
     if (e != cudaSuccess) return e;

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "decode.h"
 #include "launch.h"
 
 namespace cb {
@@ -21,10 +22,12 @@ struct Plan {
   bool fast_prefill;   // prefill rows on the tcgen05 tile kernel
   void* workspace;
   size_t workspace_bytes;
+  DecodeArgs decode;
+  DecodePlan decode_plan;
 };
 
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
-               uint32_t flags, void* workspace, size_t workspace_bytes);
+               uint32_t flags, bool scatter_first, void* workspace, size_t workspace_bytes);
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream);
 

@@ -188,3 +188,38 @@ def test_out_of_range_slot_is_recorded_and_skipped():
     torch.cuda.synchronize()
     assert torch.equal(before, st.x["k_cache"])
     assert cb.read_error_word(st.ws) & 0x2
+
+
+# ------------------------------------------------------------------ decode kernel coverage
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 8), (32, 16), (64, 8)])
+@pytest.mark.parametrize("BS", [16, 32, 256])
+def test_decode_heads_and_block_sizes(Hq, Hkv, BS):
+    rng = np.random.default_rng(Hq * 100 + Hkv + BS)
+    ctx = [int(c) for c in rng.integers(0, 3000, size=12)] + [0, 15, 16, 31]
+    spec = workloads.custom([1] * len(ctx), ctx, num_q_heads=Hq, num_kv_heads=Hkv,
+                            block_size=BS, seed=BS + Hkv)
+    full_check(spec)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("window", [0, 1, 33, 1000])
+def test_decode_split_across_ctas(D, window):
+    """Few long requests: each spans many CTAs, so the combine merges many partials."""
+    spec = workloads.custom([1, 1, 1], [20000, 9000, 300], num_q_heads=16, num_kv_heads=4,
+                            head_dim=D, seed=D + window, sliding_window=window)
+    full_check(spec)
+
+
+def test_split_merge_counters_reset_between_steps():
+    """Requests merged by their last-arriving CTA: repeated steps on one workspace agree bitwise."""
+    spec = workloads.custom([1] * 6, [30000, 5, 17000, 64, 9000, 2048], num_q_heads=64,
+                            num_kv_heads=8, seed=12)
+    st = GpuStep(spec)
+    first = st.run().clone()
+    for _ in range(3):
+        again = st.run()
+        torch.cuda.synchronize()
+        assert torch.equal(first, again)
+    assert cb.read_error_word(st.ws) == 0
