@@ -168,6 +168,45 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
  */
 cb_status cb_read_error_word(void* workspace, int32_t* h_error, void* stream);
 
+/*
+ * cb_paged_attention_no_alloc -- cb_paged_attention for callers that may not
+ * allocate device memory when they call the library: for instance a plugin
+ * inside a host program that owns the device memory pool and forbids
+ * allocations on its inference path, or a latency-critical caller that cannot
+ * pay the implicit device synchronisation of cudaMalloc/cudaFree. The pages
+ * define nothing like it: it is a deployment convenience of this library.
+ *
+ * Arguments and results are those of cb_paged_attention without the workspace
+ * pair. The scratch the step needs lives instead in one fixed device array of
+ * CB_NO_ALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads the
+ * library holds it until the process exits. The call allocates and frees
+ * nothing. A step whose plan needs more scratch than the array is rejected
+ * with CB_ERR_WORKSPACE and nothing is launched (at 8 MiB the array covers,
+ * for example, 64 decode requests with 32 query heads of size 128, or 16 with
+ * 64 heads).
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream
+ * capture. Every call shares the one array and finds it holding the previous
+ * call's contents; the call clears the part that must start at zero (error
+ * word, split-request counters) on `stream` before its kernels. Calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on the
+ * array: order them on one stream. The device error word lives in the array,
+ * so cb_read_error_word cannot read it for these calls.
+ */
+#define CB_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+cb_status cb_paged_attention_no_alloc(void* out, const void* q, void* k_cache, void* v_cache,
+                                      const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping,
+                                      const int32_t* query_start_loc, const int32_t* seq_lens,
+                                      const int32_t* block_table, int32_t block_table_stride,
+                                      const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                                      int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                                      int32_t block_size, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, float scale,
+                                      int32_t sliding_window, int32_t dtype, uint32_t flags,
+                                      void* stream);
+
 /* ---- diagnostics (no effect on results) -------------------------------- */
 
 /* Number of kernels the library has launched in this process: of kernel id

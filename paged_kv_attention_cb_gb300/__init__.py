@@ -51,6 +51,10 @@ _SIGNATURES = {
         ctypes.c_float, _i32, _i32,    # scale, sliding_window, dtype
         ctypes.c_uint32, _vp, ctypes.c_size_t, _vp]),  # flags, workspace, bytes, stream
     "cb_read_error_word": (ctypes.c_int, [_vp, _vp, _vp]),
+    "cb_paged_attention_no_alloc": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+        _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _i32, ctypes.c_uint32,
+        _vp]),
     "cb_launch_count": (ctypes.c_longlong, [ctypes.c_int]),
     "cb_num_kernels": (ctypes.c_int, []),
     "cb_kernel_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -165,6 +169,31 @@ def paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_t
         hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
         R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+NO_ALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def paged_attention_no_alloc(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                             h_query_start_loc, h_seq_lens, *, scale=0.0, sliding_window=0,
+                             k_new=None, v_new=None, slot_mapping=None, flags=0, stream=None):
+    """paged_attention without a workspace, for callers that may not allocate device memory
+    at call time (see cb_paged_attention_no_alloc in include/cb.h)."""
+    T, Hq, D = q.shape
+    NB, BS, Hkv, _ = k_cache.shape
+    R = int(seq_lens.shape[0])
+    hq = _host_i32(h_query_start_loc)
+    hs = _host_i32(h_seq_lens)
+    if hq.shape[0] != R + 1 or hs.shape[0] != R:
+        raise CbError(2, "host mirrors must have R+1 and R entries")
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    _check(lib().cb_paged_attention_no_alloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+        _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride,
+        hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
+        R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
+        _stream(stream)))
     return out
 
 

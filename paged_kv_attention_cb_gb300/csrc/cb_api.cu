@@ -39,6 +39,14 @@ cb_status check_dtype(int32_t dtype, int* elt) {
 
 }  // namespace
 
+namespace cb {
+
+// Status reporting for entry points defined in other files of the library.
+cb_status report_error(cb_status s, const char* msg) { return fail(s, msg); }
+cb_status report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+}  // namespace cb
+
 extern "C" {
 
 const char* cb_status_string(int status) {

@@ -122,6 +122,17 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
 }
 
+size_t workspace_extent(const Plan& plan, const StepArgs& a) {
+  if (!plan.fast_decode) return kWorkspaceHeaderBytes;
+  const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  const size_t slots = (size_t)a.num_requests + (size_t)plan.decode.num_ctas;
+  return w.part_o + slots * a.num_q_heads * (size_t)a.head_dim * 4;
+}
+
+size_t workspace_zeroed_prefix(const StepArgs& a) {
+  return layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim).part_ml;
+}
+
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {
   if (plan.fast_decode) {
     cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);

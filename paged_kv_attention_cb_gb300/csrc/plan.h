@@ -31,4 +31,10 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream);
 
+// Bytes at the start of the workspace that the planned launch reads or writes
+// (the rest of a cb_workspace_size() buffer is headroom for larger plans), and
+// the leading part of it that must be zero before a call (error word, counters).
+size_t workspace_extent(const Plan& plan, const StepArgs& a);
+size_t workspace_zeroed_prefix(const StepArgs& a);
+
 }  // namespace cb
