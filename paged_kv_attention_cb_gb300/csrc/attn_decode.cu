@@ -365,7 +365,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const int b_first = cta_of(u_r, U, C);
       const int b_last = cta_of(u_r + units - 1, U, C);
       const int qs = k & 1;
-      if (k >= 2 && !mbar_wait(&sm.qempty[qs], ((k >> 1) - 1) & 1)) { ok = false; break; }
+      if (k >= 2 && !mbar_wait_warp(&sm.qempty[qs], ((k >> 1) - 1) & 1)) { ok = false; break; }
       if (lane == 0) {
         SegDesc& d = sm.seg[qs];
         d.r = r;
@@ -410,7 +410,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           const int pg = __shfl_sync(0xffffffffu, cur, j);
           const int kb = kb_base + j;
           const int s = (int)(i % p.stages);
-          if (i >= p.stages && !mbar_wait(&sm.empty[s], (uint32_t)(((i / p.stages) - 1) & 1))) {
+          if (i >= p.stages && !mbar_wait_warp(&sm.empty[s], (uint32_t)(((i / p.stages) - 1) & 1))) {
             ok = false;
             break;
           }
@@ -448,7 +448,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (ok) {
       // terminator
       const int qs = k & 1;
-      if (k >= 2 && !mbar_wait(&sm.qempty[qs], ((k >> 1) - 1) & 1)) ok = false;
+      if (k >= 2 && !mbar_wait_warp(&sm.qempty[qs], ((k >> 1) - 1) & 1)) ok = false;
       if (ok && lane == 0) {
         sm.seg[qs].r = -1;
         mbar_arrive(&sm.qfull[qs]);
@@ -474,7 +474,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // last partial this CTA delivered (merged by the consumers at the end).
     int nd = 0, npend = 0;
     for (;; ++nd) {
-      if (nd >= kDoneRing || !mbar_wait(&sm.done_full[nd], 0)) {
+      if (nd >= kDoneRing || !mbar_wait_warp(&sm.done_full[nd], 0)) {
         if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
         break;
       }
@@ -511,7 +511,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   long long i = 0;
   for (int k = 0;; ++k) {
     const int qs = k & 1;
-    if (!mbar_wait(&sm.qfull[qs], (k >> 1) & 1)) {
+    if (!mbar_wait_warp(&sm.qfull[qs], (k >> 1) & 1)) {
       if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
       return;
     }
@@ -538,7 +538,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     for (int kb = d.kb0; kb < d.kb1; ++kb, ++i) {
       const int s = (int)(i % p.stages);
-      if (!mbar_wait(&sm.full[s], (uint32_t)((i / p.stages) & 1))) {
+      if (!mbar_wait_warp(&sm.full[s], (uint32_t)((i / p.stages) & 1))) {
         if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
         return;
       }
@@ -682,7 +682,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (hl == 0 && lane == 0) sm.done[nd].r = -1;
     mbar_arrive(&sm.done_full[nd]);
   }
-  if (!mbar_wait(&sm.merges_ready, 0)) {
+  if (!mbar_wait_warp(&sm.merges_ready, 0)) {
     if (lane == 0) record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
     return;
   }

@@ -1,0 +1,491 @@
+// Prefill and chunked-prefill rows (q_len > 1) of the step on tcgen05/TMEM, bf16.
+//
+// What it computes is the per-block pseudocode of "Continuous Batching"
+// (languisher.top), section "Extension: the vLLM v1 implementation", for a
+// request's query tile: context_len = seq_len - q_len, query token local_q
+// attends kv_pos 0 .. context_len + local_q (or the last sliding_window of
+// them), each resolved through block_table[req][kv_pos / BLOCK_SIZE]. The
+// chunk's own tokens were scattered into the cache before this kernel runs
+// (section "Extension: combining with chunked prefill": a chunk with a context
+// continues a prompt already in the cache). Prefill is compute-bound
+// ("Continuous batching mechanics", d9bl.com), so both products are dense
+// contractions on the 5th-generation tensor cores:
+//
+// * Tile. One CTA owns 128 query rows = 128/G tokens x the G query heads of
+//   one KV head (grouped-query packing: each K/V tile serves all G heads), and
+//   walks the request's keys in tiles of 128 up to its causal bound. Only the
+//   last tiles need the bound check; it is applied per row as a select.
+// * Staging. A TMA warp loads the Q tile once (a 3-D box over q) and each K
+//   and V tile page by page (a 4-D box per page through the block table, 128B
+//   swizzle) into a 2-stage mbarrier ring; pages past the request read as zeros.
+// * Contraction. One thread issues S = Q K^T (M 128, N 128, K = head_dim) into a
+//   double-buffered TMEM accumulator and O += P V (M 128, N = head_dim, K 128)
+//   into a TMEM accumulator, operands from swizzled shared memory (V is the
+//   N-major B operand). S of the next key tile is computed while the softmax
+//   works on the current one.
+// * Softmax. Four warps, one thread per row (= TMEM lane): load the S row with
+//   tcgen05.ld, mask, exponentiate in base 2, write P (bf16, swizzled) for the
+//   PV product. The running maximum is only raised (and O rescaled in TMEM)
+//   when it grows by more than 2^8, which keeps every P <= 256 and the result
+//   exact up to rounding. The last PV completes, O is divided by the row sum
+//   and written out.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "prefill.h"
+#include "sm100_ptx.cuh"
+
+namespace cb {
+
+namespace {
+
+constexpr int kRows = 128;             // query rows per tile
+constexpr int kKeys = 128;             // keys per key tile
+constexpr int kStages = 2;             // K/V ring depth
+constexpr int kThreads = 192;          // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr float kRescaleLog2 = 8.f;    // raise the running max only when it grows by > 2^8
+constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383
+constexpr uint32_t kTmemO = 256;
+constexpr int kHalfBytes = kRows * 128;  // 128 rows x 64 bf16 (one swizzle-atom column)
+constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys
+
+struct PfBars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+};
+
+struct Tile {
+  int r, g, qt;
+};
+
+// CTA -> (request, KV head, query tile); entries are sorted heaviest first and
+// each request's tiles are taken last tile first (the last tile has the most keys).
+CB_DEV Tile tile_of(const PrefillArgs& p, int cta) {
+  const int Hkv = p.a.num_kv_heads;
+  int base = 0;
+  for (int e = 0; e < p.n_entries; ++e) {
+    const int n = p.entries[e].n_qtiles * Hkv;
+    if (cta < base + n) {
+      const int k = cta - base;
+      return Tile{p.entries[e].r, k % Hkv, p.entries[e].n_qtiles - 1 - k / Hkv};
+    }
+    base += n;
+  }
+  return Tile{-1, 0, 0};
+}
+
+template <int D>
+__host__ __device__ constexpr int kv_bytes() {
+  return (D / 64) * kHalfBytes;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                    const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ PrefillArgs p) {
+  static_assert(D == 64 || D == 128, "head_dim");
+  constexpr int kHalves = D / 64;
+  constexpr int kKV = kv_bytes<D>();
+  constexpr int kQBytes = kHalves * kHalfBytes;
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sK = sQ + kQBytes;
+  uint8_t* sV = sK + kStages * kKV;
+  uint8_t* sP = sV + kStages * kKV;
+  PfBars& bar = *reinterpret_cast<PfBars*>(sP + kPBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Tile tile = tile_of(p, blockIdx.x);
+  if (tile.r < 0) return;  // uniform over the CTA, before any barrier
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar.s_full[b], 1);
+      mbar_init(&bar.s_free[b], 4);
+    }
+    mbar_init(&bar.p_full, 4);
+    mbar_init(&bar.o_done, 1);
+    mbar_init(&bar.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (warp == 5) tmem_alloc(&bar.tmem_base, kTmemCols);
+  grid_dependency_wait();  // the scatter of this step's K/V must be complete
+  tcgen05_fence_before();
+  __syncthreads();
+  tcgen05_fence_after();
+  allow_dependent_launch();
+  const uint32_t tmem = bar.tmem_base;
+
+  // ---- request geometry
+  const int r = tile.r;
+  const int g = tile.g;
+  const int q_start = __ldg(p.a.query_start_loc + r);
+  const int q_len = __ldg(p.a.query_start_loc + r + 1) - q_start;
+  const int seq = __ldg(p.a.seq_lens + r);
+  const int ctx = seq - q_len;
+  const int G = p.a.num_q_heads / p.a.num_kv_heads;
+  const int TQ = p.tile_tokens;
+  const int tok0 = tile.qt * TQ;
+  const int tok_end = min(q_len, tok0 + TQ);
+  const int W = p.a.sliding_window;
+  const int first_key = W > 0 ? max(0, ctx + tok0 - W + 1) : 0;
+  const int last_key = min(ctx + tok_end - 1, seq - 1);
+  const int kt0 = first_key / kKeys;
+  const int nkt = last_key / kKeys - kt0 + 1;
+  bool ok = true;
+
+  if (warp == 4) {
+    // =================================================== TMA warp
+    const int BS = p.a.block_size;
+    const int box = p.box_keys;
+    const int ppt = kKeys / box;  // pages per key tile
+    const int npages_req = (seq + BS - 1) / BS;
+    const int32_t* bt = p.a.block_table + (long long)r * p.a.bt_stride;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar.q_full, (uint32_t)kQBytes);
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h)
+        tma_load_3d(sQ + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G, q_start + tok0);
+    }
+    int issued = 0;
+    for (int j = 0; j < nkt; ++j) {
+      const int kt = kt0 + j;
+      const int s = j % kStages;
+      const int lp0 = (kt * kKeys) / BS;
+      int pg = p.a.num_blocks;  // past the pool: the TMA fills zeros
+      if (lane < ppt && lp0 + lane < npages_req) {
+        pg = __ldg(bt + lp0 + lane);
+        if (pg < 0 || pg >= p.a.num_blocks) {
+          record_error(p.a.error_word, 0x1);
+          pg = p.a.num_blocks;
+        }
+      }
+      if (j >= kStages && !mbar_wait_warp(&bar.kv_empty[s], (uint32_t)(((j / kStages) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[s], (uint32_t)(2 * kKV));
+      const int key0 = BS > kKeys ? (kt * kKeys) % BS : 0;
+      for (int i = 0; i < ppt; ++i) {
+        const int pgi = __shfl_sync(0xffffffffu, pg, i);
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h) {
+            const int off = s * kKV + h * kHalfBytes + i * box * 128;
+            tma_load_4d(sK + off, &tmap_k, &bar.kv_full[s], h * 64, key0, g, pgi);
+            tma_load_4d(sV + off, &tmap_v, &bar.kv_full[s], h * 64, key0, g, pgi);
+          }
+        }
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    if (!ok && lane == 0) {
+      record_error(p.a.error_word, 0x4);
+      // the copies already issued land before the CTA's shared memory is released
+      mbar_wait(&bar.q_full, 0);
+      for (int jj = issued > kStages ? issued - kStages : 0; jj < issued; ++jj)
+        mbar_wait(&bar.kv_full[jj % kStages], (uint32_t)((jj / kStages) & 1));
+    }
+  } else if (warp == 5) {
+    // =================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = umma_idesc_bf16(kRows, kKeys, false);
+      constexpr uint32_t idO = umma_idesc_bf16(kRows, D, true);
+      if (!mbar_wait(&bar.q_full, 0)) ok = false;
+      for (int j = 0; j <= nkt && ok; ++j) {
+        if (j < nkt) {
+          // S_j = Q K_j^T into S buffer j % 2
+          const int sb = j & 1;
+          const int s = j % kStages;
+          if (j >= 2 && !mbar_wait(&bar.s_free[sb], (uint32_t)(((j >> 1) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&bar.kv_full[s], (uint32_t)((j / kStages) & 1))) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t qa = smem_u32(sQ) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            const uint32_t ka = smem_u32(sK + s * kKV) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            umma_bf16(tmem + sb * kKeys, umma_desc_sw128(qa, 16, 1024),
+                      umma_desc_sw128(ka, 16, 1024), idS, ks > 0);
+          }
+          umma_commit(&bar.s_full[sb]);
+        }
+        if (j >= 1) {
+          // O += P_{j-1} V_{j-1}
+          const int jj = j - 1;
+          const int s = jj % kStages;
+          if (!mbar_wait(&bar.p_full, (uint32_t)(jj & 1))) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint32_t pa = smem_u32(sP) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            const uint32_t va = smem_u32(sV + s * kKV) + ks * 2048;
+            umma_bf16(tmem + kTmemO, umma_desc_sw128(pa, 16, 1024),
+                      umma_desc_sw128(va, kHalfBytes, 1024), idO, (jj > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&bar.o_done);
+          umma_commit(&bar.kv_empty[s]);
+        }
+      }
+      if (!ok) record_error(p.a.error_word, 0x4);
+      // every MMA this thread issued has completed before the TMEM is released
+      umma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // =================================================== softmax warps
+    const int row = threadIdx.x;  // TMEM lane = tile row
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    const int tok = tok0 + row / G;
+    const int hh = row % G;
+    const bool row_valid = tok < q_len;
+    const int qpos = ctx + tok;
+    const int max_kv = min(qpos, seq - 1);
+    const int min_kv = W > 0 ? max(0, qpos - W + 1) : 0;
+    const float sl2 = p.a.scale_log2;
+    float m_ref = -FLT_MAX;
+    float l = 0.f;
+    for (int j = 0; j < nkt; ++j) {
+      const int kt = kt0 + j;
+      const int sb = j & 1;
+      const int s = j % kStages;
+      if (!mbar_wait_warp(&bar.s_full[sb], (uint32_t)((j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tcgen05_fence_after();
+      uint32_t sr[kKeys];
+#pragma unroll
+      for (int c0 = 0; c0 < kKeys; c0 += 32)
+        tmem_ld32(tmem + lane_addr + sb * kKeys + c0, *reinterpret_cast<uint32_t(*)[32]>(sr + c0));
+      tmem_wait_ld();
+      float* sv = reinterpret_cast<float*>(sr);
+      tcgen05_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+      // mask (bounds only) and row maximum, base-2 scaled
+      const int key_base = kt * kKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        const int key = key_base + c;
+        const float v = (key >= min_kv && key <= max_kv) ? sv[c] * sl2 : -INFINITY;
+        sv[c] = v;
+        mx = fmaxf(mx, v);
+      }
+      const bool need = mx > m_ref + kRescaleLog2;
+      const float alpha = need ? exp2f(m_ref - mx) : 1.f;
+      if (need) m_ref = mx;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        sv[c] = exp2f(sv[c] - m_ref);
+        sum += sv[c];
+      }
+      l = l * alpha + sum;
+      // P and O belong to the previous PV product until it completes
+      if (j >= 1) {
+        if (!mbar_wait_warp(&bar.o_done, (uint32_t)((j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tcgen05_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o32[32];
+            tmem_ld32(tmem + lane_addr + kTmemO + c0, o32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+            tmem_st32(tmem + lane_addr + kTmemO + c0, o32);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row (bf16, 128B swizzle, K-major A operand of the PV product)
+#pragma unroll
+      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
+        uint4 v;
+        v.x = pack_bf16x2(sv[c8 * 8 + 0], sv[c8 * 8 + 1]);
+        v.y = pack_bf16x2(sv[c8 * 8 + 2], sv[c8 * 8 + 3]);
+        v.z = pack_bf16x2(sv[c8 * 8 + 4], sv[c8 * 8 + 5]);
+        v.w = pack_bf16x2(sv[c8 * 8 + 6], sv[c8 * 8 + 7]);
+        const int half = c8 >> 3;
+        const int chunk = c8 & 7;
+        *reinterpret_cast<uint4*>(sP + half * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+            v;
+      }
+      // V rows past the end of the sequence hold unrelated data: zero them so
+      // that 0 * V cannot produce a NaN (row index = key index in the tile)
+      if (key_base + kKeys > seq) {
+        if (!mbar_wait_warp(&bar.kv_full[s], (uint32_t)((j / kStages) & 1))) {
+          ok = false;
+          break;
+        }
+        if (key_base + row >= seq) {
+#pragma unroll
+          for (int h = 0; h < kHalves; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(sV + s * kKV + h * kHalfBytes + row * 128 + c * 16) =
+                  make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tcgen05_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_full);
+    }
+    // ---- epilogue: O / l for the rows of this tile
+    if (ok && !mbar_wait_warp(&bar.o_done, (uint32_t)((nkt - 1) & 1))) ok = false;
+    if (ok) {
+      tcgen05_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.a.out) +
+                            ((long long)(q_start + tok) * p.a.num_q_heads + g * G + hh) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o32[32];
+        tmem_ld32(tmem + lane_addr + kTmemO + c0, o32);
+        tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 0]) * inv, __uint_as_float(o32[c8 * 8 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 2]) * inv, __uint_as_float(o32[c8 * 8 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 4]) * inv, __uint_as_float(o32[c8 * 8 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 6]) * inv, __uint_as_float(o32[c8 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c0 + c8 * 8) = v;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      record_error(p.a.error_word, 0x4);
+    }
+  }
+
+  // ---- teardown: every tcgen05 access is complete before the columns are freed
+  tcgen05_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tcgen05_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+cudaError_t encode(CUtensorMap* map, void* ptr, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
+  const StepArgs& a = p.a;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const cuuint64_t e = 2;
+  CUtensorMap mq, mk, mv;
+  // q as (d, head, token); box: 64 of d, the G heads of one KV head, the tile's tokens
+  cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
+  cuuint64_t qs[2] = {(cuuint64_t)D * e, (cuuint64_t)a.num_q_heads * D * e};
+  cuuint32_t qb[3] = {64, (cuuint32_t)G, (cuuint32_t)p.tile_tokens};
+  cudaError_t err = encode(&mq, const_cast<void*>(a.q), 3, qd, qs, qb);
+  // caches as (d, key in page, head, page); box: 64 of d, box_keys keys, one head, one page
+  cuuint64_t cd[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size, (cuuint64_t)a.num_kv_heads,
+                      (cuuint64_t)a.num_blocks};
+  cuuint64_t cs[3] = {(cuuint64_t)a.num_kv_heads * D * e, (cuuint64_t)D * e,
+                      (cuuint64_t)a.block_size * a.num_kv_heads * D * e};
+  cuuint32_t cb_[4] = {64, (cuuint32_t)p.box_keys, 1, 1};
+  if (err == cudaSuccess) err = encode(&mk, a.k_cache, 4, cd, cs, cb_);
+  if (err == cudaSuccess) err = encode(&mv, a.v_cache, 4, cd, cs, cb_);
+  if (err != cudaSuccess) return err;
+  auto kern = prefill_tile_kernel<D>;
+  static bool attr_set = false;
+  const size_t smem = prefill_smem_bytes(D);
+  if (!attr_set) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mq, mk, mv, p);
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes(int head_dim) {
+  const size_t kv = (size_t)(head_dim / 64) * kHalfBytes;
+  size_t b = 1024 + kv /* Q */ + 2 * kStages * kv + kPBytes + sizeof(PfBars);
+  // at least ~half the SM's shared memory, so that a second CTA (and a second
+  // 512-column TMEM allocation) never lands on the same SM
+  if (b < 120 * 1024) b = 120 * 1024;
+  return b;
+}
+
+cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream) {
+  if (p.total_ctas <= 0) return cudaSuccess;
+  if (p.a.head_dim == 64) return launch_d<64>(p, stream);
+  return launch_d<128>(p, stream);
+}
+
+}  // namespace cb

@@ -6,6 +6,8 @@
 // the prefill kernel, and whatever the fast kernels do not cover to the
 // portable kernel.
 #include <algorithm>
+#include <utility>
+#include <vector>
 
 #include "cb.h"
 #include "decode.h"
@@ -16,6 +18,7 @@ namespace cb {
 namespace {
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr int kRowsPerTile = 128;  // query rows (tokens x grouped heads) per prefill tile
 
 int sm_count() {
   static int cached[64] = {0};
@@ -65,6 +68,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   plan.workspace_bytes = workspace_bytes;
   plan.fast_decode = false;
   plan.fast_prefill = false;
+  plan.n_prefill_launches = 0;
   plan.portable_mode = 0;
   if ((flags & CB_FLAG_PORTABLE_ONLY) || a.dtype == CB_F32) return;
 
@@ -119,7 +123,43 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
     if (d.stages >= 2) plan.fast_decode = true;
   }
-  if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
+
+  // ---- prefill rows: tcgen05 tile kernel, heaviest requests first
+  const bool prefill_ok = has_prefill && a.block_size % 8 == 0 && G <= 16 && kRowsPerTile % G == 0;
+  if (prefill_ok) {
+    const int TQ = kRowsPerTile / G;
+    std::vector<std::pair<long long, int>> order;  // (weight, r)
+    for (int r = 0; r < a.num_requests; ++r) {
+      const int ql = h_qsl[r + 1] - h_qsl[r];
+      if (ql > 1) order.emplace_back(-(long long)h_seq_lens[r] * ql, r);
+    }
+    std::stable_sort(order.begin(), order.end());
+    const int n_launch = (int)((order.size() + kPrefillMaxEntries - 1) / kPrefillMaxEntries);
+    if (n_launch <= kMaxPrefillLaunches) {
+      for (int l = 0; l < n_launch; ++l) {
+        PrefillArgs& pa = plan.prefill[l];
+        pa.a = a;
+        pa.tile_tokens = TQ;
+        pa.box_keys = std::min(a.block_size, 128);
+        pa.n_entries = 0;
+        pa.total_ctas = 0;
+        for (size_t i = (size_t)l * kPrefillMaxEntries;
+             i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
+          const int r = order[i].second;
+          const int ql = h_qsl[r + 1] - h_qsl[r];
+          PrefillEntry& e = pa.entries[pa.n_entries++];
+          e.r = r;
+          e.n_qtiles = (ql + TQ - 1) / TQ;
+          pa.total_ctas += e.n_qtiles * a.num_kv_heads;
+        }
+      }
+      plan.n_prefill_launches = n_launch;
+      plan.fast_prefill = true;
+    }
+  }
+  if (plan.fast_decode && plan.fast_prefill) plan.portable_mode = -1;
+  else if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
+  else if (plan.fast_prefill) plan.portable_mode = U > 0 ? 1 : -1;
 }
 
 size_t workspace_extent(const Plan& plan, const StepArgs& a) {
@@ -136,6 +176,10 @@ size_t workspace_zeroed_prefix(const StepArgs& a) {
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {
   if (plan.fast_decode) {
     cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);
+    if (e != cudaSuccess) return e;
+  }
+  for (int l = 0; l < plan.n_prefill_launches && plan.fast_prefill; ++l) {
+    cudaError_t e = launch_prefill(plan.prefill[l], stream);
     if (e != cudaSuccess) return e;
   }
   if (plan.portable_mode >= 0) {

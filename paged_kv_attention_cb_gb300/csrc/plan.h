@@ -6,12 +6,14 @@
 #include <stdint.h>
 
 #include "decode.h"
+#include "prefill.h"
 #include "launch.h"
 
 namespace cb {
 
 constexpr size_t kWorkspaceHeaderBytes = 256;  // error word + reserved
 constexpr int kMaxDecodeCtas = 2048;           // upper bound on decode CTAs (workspace sizing)
+constexpr int kMaxPrefillLaunches = 8;         // x kPrefillMaxEntries prefill requests per step
 
 size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim);
@@ -24,6 +26,8 @@ struct Plan {
   size_t workspace_bytes;
   DecodeArgs decode;
   DecodePlan decode_plan;
+  int n_prefill_launches;
+  PrefillArgs prefill[kMaxPrefillLaunches];
 };
 
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,

@@ -223,3 +223,35 @@ def test_split_merge_counters_reset_between_steps():
         torch.cuda.synchronize()
         assert torch.equal(first, again)
     assert cb.read_error_word(st.ws) == 0
+
+
+# ------------------------------------------------------------------ prefill tile kernel coverage
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("BS", [8, 32, 256])
+def test_prefill_groups_and_block_sizes(G, BS):
+    Hkv = 2
+    spec = workloads.custom([2, 37, 130, 300], [0, 200, 5, 1000], num_q_heads=G * Hkv,
+                            num_kv_heads=Hkv, block_size=BS, seed=G * 7 + BS)
+    full_check(spec)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("window", [0, 50, 300])
+def test_prefill_chunks_with_context(D, window):
+    """A prompt continued in chunks: context in the cache, own tokens through slot_mapping."""
+    spec = workloads.custom([129, 256, 64], [3000, 0, 700], num_q_heads=16, num_kv_heads=4,
+                            head_dim=D, seed=D + window, sliding_window=window)
+    full_check(spec)
+
+
+def test_prefill_fast_equals_portable_path():
+    spec = workloads.custom([1, 70, 1, 200], [90, 400, 3, 0], num_q_heads=32, num_kv_heads=8,
+                            seed=17)
+    st = GpuStep(spec)
+    fast = st.run().float()
+    port = st.run(flags=cb.CB_FLAG_PORTABLE_ONLY).float()
+    torch.cuda.synchronize()
+    err = (fast - port).abs()
+    assert float(err.max()) <= 2e-2 and float(err.mean()) <= 2e-3
