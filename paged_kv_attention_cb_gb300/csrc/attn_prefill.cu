@@ -17,7 +17,9 @@
 //   last tiles need the bound check; it is applied per row as a select.
 // * Staging. A TMA warp loads the Q tile once (a 3-D box over q) and each K
 //   and V tile page by page (a 4-D box per page through the block table, 128B
-//   swizzle) into a 2-stage mbarrier ring; pages past the request read as zeros.
+//   swizzle, one lane per page) into mbarrier rings (K: 3 stages, freed when S
+//   is done; V: 2 stages, freed when PV is done); pages past the request read
+//   as zeros.
 // * Contraction. One thread issues S = Q K^T (M 128, N 128, K = head_dim) into a
 //   double-buffered TMEM accumulator and O += P V (M 128, N = head_dim, K 128)
 //   into a TMEM accumulator, operands from swizzled shared memory (V is the
@@ -44,7 +46,8 @@ namespace {
 
 constexpr int kRows = 128;             // query rows per tile
 constexpr int kKeys = 128;             // keys per key tile
-constexpr int kStages = 2;             // K/V ring depth
+constexpr int kKStages = 3;            // K ring depth (K is free once S = Q K^T is done)
+constexpr int kVStages = 2;            // V ring depth (V is free once O += P V is done)
 constexpr int kThreads = 192;          // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr float kRescaleLog2 = 8.f;    // raise the running max only when it grows by > 2^8
 constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383
@@ -54,8 +57,10 @@ constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys
 
 struct PfBars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
@@ -106,8 +111,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sK = sQ + kQBytes;
-  uint8_t* sV = sK + kStages * kKV;
-  uint8_t* sP = sV + kStages * kKV;
+  uint8_t* sV = sK + kKStages * kKV;
+  uint8_t* sP = sV + kVStages * kKV;
   PfBars& bar = *reinterpret_cast<PfBars*>(sP + kPBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -117,9 +122,13 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar.kv_full[s], 1);
-      mbar_init(&bar.kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar.s_full[b], 1);
@@ -174,45 +183,71 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int h = 0; h < kHalves; ++h)
         tma_load_3d(sQ + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G, q_start + tok0);
     }
-    int issued = 0;
-    for (int j = 0; j < nkt; ++j) {
-      const int kt = kt0 + j;
-      const int s = j % kStages;
-      const int lp0 = (kt * kKeys) / BS;
+    // page ids of key tile j (lane i < ppt: page i of the tile)
+    auto tile_pages = [&](int j) -> int {
+      const int lp = (kt0 + j) * kKeys / BS + lane;
       int pg = p.a.num_blocks;  // past the pool: the TMA fills zeros
-      if (lane < ppt && lp0 + lane < npages_req) {
-        pg = __ldg(bt + lp0 + lane);
+      if (lane < ppt && lp < npages_req) {
+        pg = __ldg(bt + lp);
         if (pg < 0 || pg >= p.a.num_blocks) {
           record_error(p.a.error_word, 0x1);
           pg = p.a.num_blocks;
         }
       }
-      if (j >= kStages && !mbar_wait_warp(&bar.kv_empty[s], (uint32_t)(((j / kStages) - 1) & 1))) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&bar.kv_full[s], (uint32_t)(2 * kKV));
-      const int key0 = BS > kKeys ? (kt * kKeys) % BS : 0;
-      for (int i = 0; i < ppt; ++i) {
-        const int pgi = __shfl_sync(0xffffffffu, pg, i);
-        if (lane == 0) {
+      return pg;
+    };
+    // one tensor's key tile j into `dst`: lane i issues the boxes of page i
+    // (copies issued from several lanes proceed in parallel)
+    auto issue_tile = [&](int j, int pg, const CUtensorMap* map, uint8_t* dst, uint64_t* full) {
+      const int key0 = BS > kKeys ? ((kt0 + j) * kKeys) % BS : 0;
+      __syncwarp();  // the expect_tx above is registered first
+      if (lane < ppt) {
 #pragma unroll
-          for (int h = 0; h < kHalves; ++h) {
-            const int off = s * kKV + h * kHalfBytes + i * box * 128;
-            tma_load_4d(sK + off, &tmap_k, &bar.kv_full[s], h * 64, key0, g, pgi);
-            tma_load_4d(sV + off, &tmap_v, &bar.kv_full[s], h * 64, key0, g, pgi);
-          }
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_4d(dst + h * kHalfBytes + lane * box * 128, map, full, h * 64, key0, g, pg);
+      }
+    };
+    // K runs one tile ahead of V; page ids are read one tile ahead
+    int k_issued = 0, v_issued = 0;
+    int ids_next = tile_pages(0);
+    int ids_v = 0;
+    for (int j = -1; j < nkt && ok; ++j) {
+      const int jk = j + 1;
+      const int ids_k = ids_next;
+      if (jk + 1 < nkt) ids_next = tile_pages(jk + 1);
+      if (jk < nkt) {
+        const int s = jk % kKStages;
+        if (jk >= kKStages &&
+            !mbar_wait_warp(&bar.k_empty[s], (uint32_t)(((jk / kKStages) - 1) & 1))) {
+          ok = false;
+          break;
         }
+        if (lane == 0) mbar_arrive_expect_tx(&bar.k_full[s], (uint32_t)kKV);
+        issue_tile(jk, ids_k, &tmap_k, sK + s * kKV, &bar.k_full[s]);
+        k_issued = jk + 1;
+      }
+      if (j >= 0) {
+        const int s = j % kVStages;
+        if (j >= kVStages &&
+            !mbar_wait_warp(&bar.v_empty[s], (uint32_t)(((j / kVStages) - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full[s], (uint32_t)kKV);
+        issue_tile(j, ids_v, &tmap_v, sV + s * kKV, &bar.v_full[s]);
+        v_issued = j + 1;
       }
       __syncwarp();
-      issued = j + 1;
+      ids_v = ids_k;
     }
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
       // the copies already issued land before the CTA's shared memory is released
       mbar_wait(&bar.q_full, 0);
-      for (int jj = issued > kStages ? issued - kStages : 0; jj < issued; ++jj)
-        mbar_wait(&bar.kv_full[jj % kStages], (uint32_t)((jj / kStages) & 1));
+      for (int jj = k_issued > kKStages ? k_issued - kKStages : 0; jj < k_issued; ++jj)
+        mbar_wait(&bar.k_full[jj % kKStages], (uint32_t)((jj / kKStages) & 1));
+      for (int jj = v_issued > kVStages ? v_issued - kVStages : 0; jj < v_issued; ++jj)
+        mbar_wait(&bar.v_full[jj % kVStages], (uint32_t)((jj / kVStages) & 1));
     }
   } else if (warp == 5) {
     // =================================================== MMA issuer
@@ -224,12 +259,12 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (j < nkt) {
           // S_j = Q K_j^T into S buffer j % 2
           const int sb = j & 1;
-          const int s = j % kStages;
+          const int s = j % kKStages;
           if (j >= 2 && !mbar_wait(&bar.s_free[sb], (uint32_t)(((j >> 1) - 1) & 1))) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&bar.kv_full[s], (uint32_t)((j / kStages) & 1))) {
+          if (!mbar_wait(&bar.k_full[s], (uint32_t)((j / kKStages) & 1))) {
             ok = false;
             break;
           }
@@ -242,12 +277,14 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       umma_desc_sw128(ka, 16, 1024), idS, ks > 0);
           }
           umma_commit(&bar.s_full[sb]);
+          umma_commit(&bar.k_empty[s]);
         }
         if (j >= 1) {
           // O += P_{j-1} V_{j-1}
           const int jj = j - 1;
-          const int s = jj % kStages;
-          if (!mbar_wait(&bar.p_full, (uint32_t)(jj & 1))) {
+          const int s = jj % kVStages;
+          if (!mbar_wait(&bar.p_full, (uint32_t)(jj & 1)) ||
+              !mbar_wait(&bar.v_full[s], (uint32_t)((jj / kVStages) & 1))) {
             ok = false;
             break;
           }
@@ -260,7 +297,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       umma_desc_sw128(va, kHalfBytes, 1024), idO, (jj > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(&bar.o_done);
-          umma_commit(&bar.kv_empty[s]);
+          umma_commit(&bar.v_empty[s]);
         }
       }
       if (!ok) record_error(p.a.error_word, 0x4);
@@ -280,12 +317,14 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int max_kv = min(qpos, seq - 1);
     const int min_kv = W > 0 ? max(0, qpos - W + 1) : 0;
     const float sl2 = p.a.scale_log2;
+    // keys every row of the tile attends: [tile_min_kv_max, tile_max_kv_min]
+    const int tile_max_kv_min = min(ctx + tok0, seq - 1);
+    const int tile_min_kv_max = W > 0 ? max(0, ctx + tok_end - 1 - W + 1) : 0;
     float m_ref = -FLT_MAX;
     float l = 0.f;
     for (int j = 0; j < nkt; ++j) {
       const int kt = kt0 + j;
       const int sb = j & 1;
-      const int s = j % kStages;
       if (!mbar_wait_warp(&bar.s_full[sb], (uint32_t)((j >> 1) & 1))) {
         ok = false;
         break;
@@ -300,25 +339,37 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tcgen05_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.s_free[sb]);
-      // mask (bounds only) and row maximum, base-2 scaled
+      // mask (bounds only; tiles inside every row's range need none) and row
+      // maximum of the raw scores (the scale is positive, so it commutes with max)
       const int key_base = kt * kKeys;
-      float mx = -INFINITY;
+      if (key_base < tile_min_kv_max || key_base + kKeys - 1 > tile_max_kv_min) {
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const int key = key_base + c;
-        const float v = (key >= min_kv && key <= max_kv) ? sv[c] * sl2 : -INFINITY;
-        sv[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < kKeys; ++c) {
+          const int key = key_base + c;
+          if (key < min_kv || key > max_kv) sv[c] = -INFINITY;
+        }
       }
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
+#pragma unroll
+      for (int c = 8; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
       const bool need = mx > m_ref + kRescaleLog2;
-      const float alpha = need ? exp2f(m_ref - mx) : 1.f;
+      const float alpha = need ? ex2_approx(m_ref - mx) : 1.f;
       if (need) m_ref = mx;
-      float sum = 0.f;
+      // p = 2^(s * scale_log2 - m): one FFMA and one SFU op per score
+      float sum8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
 #pragma unroll
       for (int c = 0; c < kKeys; ++c) {
-        sv[c] = exp2f(sv[c] - m_ref);
-        sum += sv[c];
+        sv[c] = ex2_approx(fmaf(sv[c], sl2, -m_ref));
+        sum8[c & 7] += sv[c];
       }
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) +
+                        ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + sum;
       // P and O belong to the previous PV product until it completes
       if (j >= 1) {
@@ -356,7 +407,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // V rows past the end of the sequence hold unrelated data: zero them so
       // that 0 * V cannot produce a NaN (row index = key index in the tile)
       if (key_base + kKeys > seq) {
-        if (!mbar_wait_warp(&bar.kv_full[s], (uint32_t)((j / kStages) & 1))) {
+        if (!mbar_wait_warp(&bar.v_full[j % kVStages], (uint32_t)((j / kVStages) & 1))) {
           ok = false;
           break;
         }
@@ -365,7 +416,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
           for (int h = 0; h < kHalves; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(sV + s * kKV + h * kHalfBytes + row * 128 + c * 16) =
+              *reinterpret_cast<uint4*>(sV + (j % kVStages) * kKV + h * kHalfBytes + row * 128 + c * 16) =
                   make_uint4(0, 0, 0, 0);
         }
       }
@@ -475,7 +526,7 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
 
 size_t prefill_smem_bytes(int head_dim) {
   const size_t kv = (size_t)(head_dim / 64) * kHalfBytes;
-  size_t b = 1024 + kv /* Q */ + 2 * kStages * kv + kPBytes + sizeof(PfBars);
+  size_t b = 1024 + kv /* Q */ + (kKStages + kVStages) * kv + kPBytes + sizeof(PfBars);
   // at least ~half the SM's shared memory, so that a second CTA (and a second
   // 512-column TMEM allocation) never lands on the same SM
   if (b < 120 * 1024) b = 120 * 1024;
