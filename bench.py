@@ -12,8 +12,10 @@ block_size 16, bf16.
 Reported metric: achieved KV-read HBM bandwidth (algorithmic KV bytes of the
 step, every attended position of every request counted once, over the step's
 device time) and query tokens/s, with the roofline of the dominant kernel
-against the measured HBM copy bandwidth. L2 is flushed (a 512 MiB write)
-between timed steps. With N > 1 (torchrun), every rank runs an independent
+against the measured HBM copy bandwidth. The step's KV is larger than L2
+(129 MB); between timed steps a 512 MiB read evicts the previous step's lines
+and leaves L2 clean (``--flush write`` writes 512 MiB instead, which leaves
+dirty lines whose write-back then competes with the step's reads). With N > 1 (torchrun), every rank runs an independent
 replica of the step (the path needs no exchange) and the job value is the sum
 of the bytes over the slowest rank's time.
 
@@ -206,8 +208,17 @@ def run_ours(args, spec, world, rank, local):
     ws = cb.alloc_workspace(spec.R, spec.T, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                             dev)
     out = torch.empty_like(x["q"])
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    class Flush:
+        def fill_(self, v):
+            if args.flush == "write":
+                flush_buf.fill_(v)
+            else:
+                flush_buf.max()  # reads every line; the result is discarded
+
+    flush = Flush()
 
     def step():
         cb.paged_attention(out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
@@ -242,6 +253,19 @@ def run_ours(args, spec, world, rank, local):
     local_ms = sum(step_ms)
     total_ms = reduce_max(local_ms, world)
     ms_per_step = total_ms / args.steps
+
+    # ---- the same steps after a dirty (write) flush, for comparison
+    alt_ms = None
+    if args.flush == "read":
+        a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            a0[i].record(stream)
+            step()
+            a1[i].record(stream)
+        torch.cuda.synchronize()
+        alt_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(a0, a1)), world) / args.steps
 
     # ---- per-kernel attribution pass (same steps, events around each launch)
     cb.kernel_timing(True)
@@ -288,7 +312,7 @@ def run_ours(args, spec, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world)
     barrier(world)
-    return dict(ms_per_step=ms_per_step, step_ms=step_ms, launches=launches,
+    return dict(ms_per_step=ms_per_step, step_ms=step_ms, launches=launches, alt_ms=alt_ms,
                 per_kernel=per_kernel, e2e_ms_per_step=e2e_ms / args.steps, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary())
 
@@ -355,6 +379,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush", choices=["read", "write"], default="read",
+                    help="L2 eviction between timed steps: read (clean) or write (dirty) 512 MiB")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -367,7 +393,9 @@ def main():
            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
            "head_dim": spec.head_dim, "block_size": spec.block_size,
            "num_blocks": spec.num_blocks, "sliding_window": spec.sliding_window,
-           "kv_bytes_per_step": kvb, "l2": "flushed (512 MiB write) between timed steps",
+           "kv_bytes_per_step": kvb,
+           "l2": ("inputs larger than L2; 512 MiB read between timed steps (L2 evicted, clean)"
+                  if args.flush == "read" else "flushed (512 MiB write) between timed steps"),
            "parallelism": f"replicas x{world}"}
 
     if args.impl == "reference":
@@ -438,6 +466,8 @@ def main():
             if spec.dtype == "bf16" else "f32", "data": "synthetic", "config": cfg,
             "tokens_per_s": tok_s,
             "step_ms_median": statistics.median(res["step_ms"]),
+            "value_after_write_flush": (world * kvb / (res["alt_ms"] * 1e-3) / 1e9
+                                        if res["alt_ms"] else None),
             "e2e": {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"]},

@@ -53,6 +53,14 @@ cudaError_t launch_write_kv(const void* k_new, const void* v_new, void* k_cache,
   // grid at least a few CTAs per SM for small steps.
   const int tok_per_cta = row_vecs >= kScatterThreads ? 1 : 2;
   const int grid = (num_tokens + tok_per_cta - 1) / tok_per_cta;
+  // Prefer the shared-memory-heavy carveout the attention kernels that follow
+  // use, so the SMs are not reconfigured between the two launches.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(write_kv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
   return launch_pdl(kWriteKv, write_kv_kernel, dim3(grid), dim3(kScatterThreads), 0, stream,
                     static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                     static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping,
