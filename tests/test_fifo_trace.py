@@ -1,0 +1,115 @@
+"""Host-side FIFO step-trace generator (the scheduler and page allocator that feed the
+hot path), checked on the CPU against the schedules the pages describe."""
+import numpy as np
+
+from workloads import RESERVED_PAGES
+from workloads.fifo_trace import (FifoScheduler, Request, TraceConfig, fifo_trace, to_spec)
+
+
+def run(cfg, requests, max_steps=100000):
+    s = FifoScheduler(cfg, requests)
+    batches = []
+    while not s.done() and s.step_index < max_steps:
+        b = s.schedule()
+        batches.append([(r.rid, c, q) for r, c, q in b])
+        s.complete(b)
+    return s, batches
+
+
+def test_slot_example_of_the_tutorial():
+    """Four slots; A, B, C, D, E need 100, 20, 50, 200, 30 output tokens, one step each:
+    E takes B's slot when B finishes at step 20 and finishes at step 50; D ends at 200."""
+    cfg = TraceConfig(max_requests_per_batch=4, max_batch_tokens=1 << 20, num_pages=4096,
+                      safety_margin=0.0)
+    outs = [100, 20, 50, 200, 30]
+    reqs = [Request(i, 1, n, 0) for i, n in enumerate(outs)]
+    s, batches = run(cfg, reqs)
+    finish = {r.rid: r.finish_step + 1 for r in s.finished}  # 1-based step numbers
+    assert finish == {0: 100, 1: 20, 2: 50, 3: 200, 4: 50}
+    assert len(batches) == 200
+    assert all(len(b) <= 4 for b in batches)
+    assert [rid for rid, _, _ in batches[20]].count(4) == 1 and 4 not in [x[0] for x in batches[19]]
+
+
+def test_fifo_priority_decode_then_prefill_then_waiting():
+    cfg = TraceConfig(max_batch_tokens=64, max_requests_per_batch=16, num_pages=1024,
+                      safety_margin=0.0)
+    reqs = [Request(0, 8, 5, 0), Request(1, 100, 5, 0), Request(2, 10, 5, 1),
+            Request(3, 10, 5, 1)]
+    s = FifoScheduler(cfg, reqs)
+    b0 = s.schedule()  # step 0: request 0 whole, request 1 chunked to the budget
+    assert [(r.rid, c, q) for r, c, q in b0] == [(0, 0, 8), (1, 0, 56)]
+    s.complete(b0)
+    b1 = s.schedule()  # decode of 0, then 1's next chunk, then arrivals 2, 3 in order
+    assert [(r.rid, c, q) for r, c, q in b1] == [(0, 8, 1), (1, 56, 44), (2, 0, 10), (3, 0, 9)]
+
+
+def test_chunked_prefill_continues_where_it_stopped():
+    cfg = TraceConfig(max_batch_tokens=4096, num_pages=4096, safety_margin=0.0)
+    s, batches = run(cfg, [Request(0, 10000, 2, 0)])
+    assert batches[:3] == [[(0, 0, 4096)], [(0, 4096, 4096)], [(0, 8192, 1808)]]
+    assert batches[3] == [(0, 10000, 1)]  # the one decode step of a 2-token output
+    assert len(batches) == 4
+
+
+def test_safety_margin_holds_new_prefills():
+    # 100 usable pages of 16 tokens; margin 0.5: a 1000-token prompt (63 pages) is admitted,
+    # leaving 37% free, so the next arrival waits while the first one decodes
+    cfg = TraceConfig(num_pages=100 + RESERVED_PAGES, block_size=16, safety_margin=0.5,
+                      max_batch_tokens=4096)
+    s = FifoScheduler(cfg, [Request(0, 1000, 3, 0), Request(1, 10, 3, 0)])
+    b0 = s.schedule()
+    assert [r.rid for r, _, _ in b0] == [0]
+    s.complete(b0)
+    b1 = s.schedule()
+    assert [r.rid for r, _, _ in b1] == [0]
+    s.complete(b1)
+    s.complete(s.schedule())  # request 0 finishes and frees its pages
+    assert [r.rid for r, _, _ in s.schedule()] == [1]
+
+
+def test_soft_reset_frees_the_newest_and_everything_finishes():
+    cfg = TraceConfig(num_pages=40 + RESERVED_PAGES, block_size=16, safety_margin=0.0,
+                      max_batch_tokens=1024)
+    reqs = [Request(i, 200, 120, 0) for i in range(3)]  # 3 x 20 pages at the end > 40
+    s, batches = run(cfg, reqs, max_steps=5000)
+    assert s.done()
+    assert sum(r.resets for r in s.finished) >= 1
+    assert s.finished[0].resets == 0  # the oldest request is never the victim here
+    assert s.pool.available() == s.pool.capacity
+
+
+def test_trace_metadata_is_consistent():
+    cfg = TraceConfig()
+    seen = 0
+    for st in fifo_trace(cfg, max_steps=60):
+        sp = st.spec
+        assert sp.T <= cfg.max_batch_tokens and sp.R <= cfg.max_requests_per_batch
+        assert list(sp.query_start_loc[1:] - sp.query_start_loc[:-1]) == list(sp.q_lens)
+        # decodes first, then prefill chunks
+        dec = sp.q_lens == 1
+        if dec.any() and (~dec).any():
+            assert np.flatnonzero(dec).max() < np.flatnonzero(~dec).min() or \
+                all(sp.ctx_lens[~dec] + sp.q_lens[~dec] <= sp.seq_lens[~dec])
+        pages = []
+        for r in range(sp.R):
+            n = -(-int(sp.seq_lens[r]) // cfg.block_size)
+            row = sp.block_table[r, :n]
+            assert row.min() >= RESERVED_PAGES and row.max() < cfg.num_pages
+            pages += list(row)
+            for i in range(int(sp.q_lens[r])):
+                p = int(sp.ctx_lens[r]) + i
+                t = int(sp.query_start_loc[r]) + i
+                assert sp.slot_mapping[t] == row[p // cfg.block_size] * cfg.block_size + p % cfg.block_size
+        assert len(pages) == len(set(pages))  # no page shared between requests
+        seen += 1
+    assert seen == 60
+
+
+def test_small_trace_runs_to_completion():
+    cfg = TraceConfig(num_requests=60, prompt_median=100, output_mean=20, arrivals_per_step=8,
+                      max_batch_tokens=512, max_requests_per_batch=32, num_pages=600)
+    steps = list(fifo_trace(cfg))
+    assert steps and steps[-1].spec.T >= 1
+    total_tokens = sum(int(st.spec.T) for st in steps)
+    assert total_tokens > 60
