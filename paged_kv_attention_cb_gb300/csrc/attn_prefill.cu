@@ -17,17 +17,18 @@
 //   last tiles need the bound check; it is applied per row as a select.
 // * Staging. A TMA warp loads the Q tile once (a 3-D box over q) and each K
 //   and V tile page by page (a 4-D box per page through the block table, 128B
-//   swizzle, one lane per page) into mbarrier rings (K: 3 stages, freed when S
+//   swizzle, one lane per page) into mbarrier rings (K: 4 stages, freed when S
 //   is done; V: 2 stages, freed when PV is done); pages past the request read
 //   as zeros.
-// * Contraction. One thread issues S = Q K^T (M 128, N 128, K = head_dim) into a
-//   double-buffered TMEM accumulator and O += P V (M 128, N = head_dim, K 128)
-//   into a TMEM accumulator, operands from swizzled shared memory (V is the
-//   N-major B operand). S of the next key tile is computed while the softmax
+// * Contraction. One thread issues S = Q K^T (M 128, N 128, K = head_dim; Q
+//   and K from swizzled shared memory) into a double-buffered TMEM accumulator,
+//   and O += P V (M 128, N = head_dim, K 128) into a TMEM accumulator with P
+//   read from TMEM where the softmax left it and V as the N-major
+//   shared-memory operand. S of the next key tile is computed while the softmax
 //   works on the current one.
 // * Softmax. Four warps, one thread per row (= TMEM lane): load the S row with
-//   tcgen05.ld, mask, exponentiate in base 2, write P (bf16, swizzled) for the
-//   PV product. The running maximum is only raised (and O rescaled in TMEM)
+//   tcgen05.ld, mask, exponentiate in base 2, write P (bf16 pairs, tcgen05.st)
+//   into TMEM for the PV product. The running maximum is only raised (and O rescaled in TMEM)
 //   when it grows by more than 2^8, which keeps every P <= 256 and the result
 //   exact up to rounding. The last PV completes, O is divided by the row sum
 //   and written out.
@@ -46,14 +47,14 @@ namespace {
 
 constexpr int kRows = 128;             // query rows per tile
 constexpr int kKeys = 128;             // keys per key tile
-constexpr int kKStages = 3;            // K ring depth (K is free once S = Q K^T is done)
+constexpr int kKStages = 4;            // K ring depth (K is free once S = Q K^T is done)
 constexpr int kVStages = 2;            // V ring depth (V is free once O += P V is done)
 constexpr int kThreads = 192;          // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr float kRescaleLog2 = 8.f;    // raise the running max only when it grows by > 2^8
-constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383
+constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383, P: 384-447
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;       // bf16 pairs: 128 keys in 64 columns
 constexpr int kHalfBytes = kRows * 128;  // 128 rows x 64 bf16 (one swizzle-atom column)
-constexpr int kPBytes = 2 * kHalfBytes;  // P: 128 rows x 128 keys
 
 struct PfBars {
   uint64_t q_full;
@@ -112,8 +113,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* sQ = base;
   uint8_t* sK = sQ + kQBytes;
   uint8_t* sV = sK + kKStages * kKV;
-  uint8_t* sP = sV + kVStages * kKV;
-  PfBars& bar = *reinterpret_cast<PfBars*>(sP + kPBytes);
+  PfBars& bar = *reinterpret_cast<PfBars*>(sV + kVStages * kKV);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -291,10 +291,10 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tcgen05_fence_after();
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks) {
-            const uint32_t pa = smem_u32(sP) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
             const uint32_t va = smem_u32(sV + s * kKV) + ks * 2048;
-            umma_bf16(tmem + kTmemO, umma_desc_sw128(pa, 16, 1024),
-                      umma_desc_sw128(va, kHalfBytes, 1024), idO, (jj > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + ks * 8,
+                             umma_desc_sw128(va, kHalfBytes, 1024), idO,
+                             (jj > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(&bar.o_done);
           umma_commit(&bar.v_empty[s]);
@@ -391,18 +391,13 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tmem_wait_st();
         }
       }
-      // P row (bf16, 128B swizzle, K-major A operand of the PV product)
+      // P row as bf16 pairs into TMEM (lane = row), the A operand of the PV product
 #pragma unroll
-      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-        uint4 v;
-        v.x = pack_bf16x2(sv[c8 * 8 + 0], sv[c8 * 8 + 1]);
-        v.y = pack_bf16x2(sv[c8 * 8 + 2], sv[c8 * 8 + 3]);
-        v.z = pack_bf16x2(sv[c8 * 8 + 4], sv[c8 * 8 + 5]);
-        v.w = pack_bf16x2(sv[c8 * 8 + 6], sv[c8 * 8 + 7]);
-        const int half = c8 >> 3;
-        const int chunk = c8 & 7;
-        *reinterpret_cast<uint4*>(sP + half * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4)) =
-            v;
+      for (int c0 = 0; c0 < kKeys; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(sv[c0 + 2 * i], sv[c0 + 2 * i + 1]);
+        tmem_st16(tmem + lane_addr + kTmemP + c0 / 2, pk);
       }
       // V rows past the end of the sequence hold unrelated data: zero them so
       // that 0 * V cannot produce a NaN (row index = key index in the tile)
@@ -419,8 +414,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
               *reinterpret_cast<uint4*>(sV + (j % kVStages) * kKV + h * kHalfBytes + row * 128 + c * 16) =
                   make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tcgen05_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.p_full);
@@ -526,7 +522,7 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
 
 size_t prefill_smem_bytes(int head_dim) {
   const size_t kv = (size_t)(head_dim / 64) * kHalfBytes;
-  size_t b = 1024 + kv /* Q */ + (kKStages + kVStages) * kv + kPBytes + sizeof(PfBars);
+  size_t b = 1024 + kv /* Q */ + (kKStages + kVStages) * kv + sizeof(PfBars);
   // at least ~half the SM's shared memory, so that a second CTA (and a second
   // 512-column TMEM allocation) never lands on the same SM
   if (b < 120 * 1024) b = 120 * 1024;
