@@ -71,23 +71,34 @@ struct PfBars {
 };
 
 struct Tile {
-  int r, g, qt;
+  int r, g, pair, qt;
+  bool shadow;  // the odd last tile's partner: loads its half of K/V, stores nothing
 };
 
-// CTA -> (request, KV head, query tile); entries are sorted heaviest first and
-// each request's tiles are taken last tile first (the last tile has the most keys).
-CB_DEV Tile tile_of(const PrefillArgs& p, int cta) {
+// Cluster -> (request, KV head, pair of query tiles); entries are sorted
+// heaviest first and each request's pairs are taken last first (the last has
+// the most keys). CTA rank 0 of the cluster takes the pair's first tile.
+CB_DEV Tile tile_of(const PrefillArgs& p, int cluster, int rank) {
   const int Hkv = p.a.num_kv_heads;
   int base = 0;
   for (int e = 0; e < p.n_entries; ++e) {
-    const int n = p.entries[e].n_qtiles * Hkv;
-    if (cta < base + n) {
-      const int k = cta - base;
-      return Tile{p.entries[e].r, k % Hkv, p.entries[e].n_qtiles - 1 - k / Hkv};
+    const int nq = p.entries[e].n_qtiles;
+    const int npairs = (nq + 1) / 2;
+    const int n = npairs * Hkv;
+    if (cluster < base + n) {
+      const int k = cluster - base;
+      Tile t;
+      t.r = p.entries[e].r;
+      t.g = k % Hkv;
+      t.pair = npairs - 1 - k / Hkv;
+      t.qt = 2 * t.pair + rank;
+      t.shadow = t.qt >= nq;
+      if (t.shadow) t.qt = nq - 1;
+      return t;
     }
     base += n;
   }
-  return Tile{-1, 0, 0};
+  return Tile{-1, 0, 0, 0, true};
 }
 
 template <int D>
@@ -117,18 +128,19 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Tile tile = tile_of(p, blockIdx.x);
+  const uint32_t rank = cluster_cta_rank();  // clusters of two CTAs share K/V loads
+  const Tile tile = tile_of(p, blockIdx.x / 2, (int)rank);
   if (tile.r < 0) return;  // uniform over the CTA, before any barrier
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bar.k_full[s], 1);
-      mbar_init(&bar.k_empty[s], 1);
+      mbar_init(&bar.k_empty[s], 2);  // released by both CTAs' S products
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bar.v_full[s], 1);
-      mbar_init(&bar.v_empty[s], 1);
+      mbar_init(&bar.v_empty[s], 2);  // released by both CTAs' PV products
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar.s_full[b], 1);
@@ -147,7 +159,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (warp == 5) tmem_alloc(&bar.tmem_base, kTmemCols);
   grid_dependency_wait();  // the scatter of this step's K/V must be complete
   tcgen05_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either multicasts into them
   tcgen05_fence_after();
   allow_dependent_launch();
   const uint32_t tmem = bar.tmem_base;
@@ -163,9 +175,12 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const int TQ = p.tile_tokens;
   const int tok0 = tile.qt * TQ;
   const int tok_end = min(q_len, tok0 + TQ);
+  // the cluster walks the union of its two tiles' key ranges
+  const int pair_tok0 = 2 * tile.pair * TQ;
+  const int pair_tok_end = min(q_len, pair_tok0 + 2 * TQ);
   const int W = p.a.sliding_window;
-  const int first_key = W > 0 ? max(0, ctx + tok0 - W + 1) : 0;
-  const int last_key = min(ctx + tok_end - 1, seq - 1);
+  const int first_key = W > 0 ? max(0, ctx + pair_tok0 - W + 1) : 0;
+  const int last_key = min(ctx + pair_tok_end - 1, seq - 1);
   const int kt0 = first_key / kKeys;
   const int nkt = last_key / kKeys - kt0 + 1;
   bool ok = true;
@@ -196,16 +211,20 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       return pg;
     };
-    // one tensor's key tile j into `dst`: lane i issues the boxes of page i
-    // (copies issued from several lanes proceed in parallel)
+    // one tensor's key tile j into `dst` of both CTAs: the tile's boxes (ppt
+    // pages x kHalves halves) are split between the two CTAs, each box
+    // multicast to both; lane i issues box 2i + rank (lanes issue in parallel)
+    const int nbox = ppt * kHalves;
     auto issue_tile = [&](int j, int pg, const CUtensorMap* map, uint8_t* dst, uint64_t* full) {
       const int key0 = BS > kKeys ? ((kt0 + j) * kKeys) % BS : 0;
+      const int bx = 2 * lane + (int)rank;
+      const int page = bx / kHalves;
+      const int half = bx % kHalves;
+      const int pgb = __shfl_sync(0xffffffffu, pg, page & 31);
       __syncwarp();  // the expect_tx above is registered first
-      if (lane < ppt) {
-#pragma unroll
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_4d(dst + h * kHalfBytes + lane * box * 128, map, full, h * 64, key0, g, pg);
-      }
+      if (bx < nbox)
+        tma_load_4d_multicast(dst + half * kHalfBytes + page * box * 128, map, full, half * 64,
+                              key0, g, pgb, (uint16_t)0x3);
     };
     // K runs one tile ahead of V; page ids are read one tile ahead
     int k_issued = 0, v_issued = 0;
@@ -277,7 +296,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       umma_desc_sw128(ka, 16, 1024), idS, ks > 0);
           }
           umma_commit(&bar.s_full[sb]);
-          umma_commit(&bar.k_empty[s]);
+          umma_commit_multicast(&bar.k_empty[s], (uint16_t)0x3);
         }
         if (j >= 1) {
           // O += P_{j-1} V_{j-1}
@@ -297,7 +316,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
                              (jj > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(&bar.o_done);
-          umma_commit(&bar.v_empty[s]);
+          umma_commit_multicast(&bar.v_empty[s], (uint16_t)0x3);
         }
       }
       if (!ok) record_error(p.a.error_word, 0x4);
@@ -312,7 +331,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
     const int tok = tok0 + row / G;
     const int hh = row % G;
-    const bool row_valid = tok < q_len;
+    const bool row_valid = tok < q_len && !tile.shadow;
     const int qpos = ctx + tok;
     const int max_kv = min(qpos, seq - 1);
     const int min_kv = W > 0 ? max(0, qpos - W + 1) : 0;
@@ -450,9 +469,11 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   }
 
-  // ---- teardown: every tcgen05 access is complete before the columns are freed
+  // ---- teardown: every tcgen05 access is complete before the columns are
+  // freed, and neither CTA leaves while the other may still write into it
   tcgen05_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 5) {
     tcgen05_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -515,7 +536,8 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mq, mk, mv, p);
+  return launch_pdl_cluster(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), 2, smem, s, mq,
+                            mk, mv, p);
 }
 
 }  // namespace

@@ -150,7 +150,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
           PrefillEntry& e = pa.entries[pa.n_entries++];
           e.r = r;
           e.n_qtiles = (ql + TQ - 1) / TQ;
-          pa.total_ctas += e.n_qtiles * a.num_kv_heads;
+          pa.total_ctas += 2 * ((e.n_qtiles + 1) / 2) * a.num_kv_heads;  // clusters of two
         }
       }
       plan.n_prefill_launches = n_launch;

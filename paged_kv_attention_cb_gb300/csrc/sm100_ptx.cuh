@@ -90,6 +90,30 @@ CB_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       : "memory");
 }
 
+// The same tile into the shared memory of every CTA in `cta_mask` (same offset in
+// each), completing bytes on the mbarrier at `bar`'s offset in each of them.
+CB_DEV void tma_load_4d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                  int c1, int c2, int c3, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "h"(cta_mask)
+      : "memory");
+}
+
+CB_DEV uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs in the cluster (release / acquire at cluster scope).
+CB_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
 CB_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -163,6 +187,16 @@ CB_DEV void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once every
+// tcgen05.mma issued so far by this thread has completed.
+CB_DEV void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
