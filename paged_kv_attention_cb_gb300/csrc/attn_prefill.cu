@@ -15,13 +15,14 @@
 //   one KV head (grouped-query packing: each K/V tile serves all G heads), and
 //   walks the request's keys in tiles of 128 up to its causal bound. Only the
 //   last tiles need the bound check; it is applied per row as a select.
-// * Staging. A TMA warp loads the Q tile once (a 3-D box over q) and each K
-//   and V tile page by page (a 4-D box per page through the block table, 128B
+// * Staging. The softmax threads copy their query rows into TMEM once; a TMA
+//   warp loads each K and V tile page by page (a 4-D box per page through the block table, 128B
 //   swizzle, one lane per page) into mbarrier rings (K: 4 stages, freed when S
-//   is done; V: 2 stages, freed when PV is done); pages past the request read
+//   is done; V: 3 stages, freed when PV is done); pages past the request read
 //   as zeros.
 // * Contraction. One thread issues S = Q K^T (M 128, N 128, K = head_dim; Q
-//   and K from swizzled shared memory) into a double-buffered TMEM accumulator,
+//   from TMEM, K from swizzled shared memory, so only one operand streams
+//   through shared memory) into a double-buffered TMEM accumulator,
 //   and O += P V (M 128, N = head_dim, K 128) into a TMEM accumulator with P
 //   read from TMEM where the softmax left it and V as the N-major
 //   shared-memory operand. S of the next key tile is computed while the softmax
@@ -48,16 +49,17 @@ namespace {
 constexpr int kRows = 128;             // query rows per tile
 constexpr int kKeys = 128;             // keys per key tile
 constexpr int kKStages = 4;            // K ring depth (K is free once S = Q K^T is done)
-constexpr int kVStages = 2;            // V ring depth (V is free once O += P V is done)
+constexpr int kVStages = 3;            // V ring depth (V is free once O += P V is done)
 constexpr int kThreads = 192;          // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr float kRescaleLog2 = 8.f;    // raise the running max only when it grows by > 2^8
-constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383, P: 384-447
+constexpr uint32_t kTmemCols = 512;    // S0: 0-127, S1: 128-255, O: 256-383, P: 384-447, Q: 448-511
 constexpr uint32_t kTmemO = 256;
 constexpr uint32_t kTmemP = 384;       // bf16 pairs: 128 keys in 64 columns
+constexpr uint32_t kTmemQ = 448;       // bf16 pairs: head_dim <= 128 in 64 columns
 constexpr int kHalfBytes = kRows * 128;  // 128 rows x 64 bf16 (one swizzle-atom column)
 
 struct PfBars {
-  uint64_t q_full;
+  uint64_t q_full;  // Q rows stored into TMEM by the four softmax warps
   uint64_t k_full[kKStages];
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
@@ -110,19 +112,16 @@ __host__ __device__ constexpr int kv_bytes() {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                    const __grid_constant__ CUtensorMap tmap_k,
+prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __grid_constant__ PrefillArgs p) {
   static_assert(D == 64 || D == 128, "head_dim");
   constexpr int kHalves = D / 64;
   constexpr int kKV = kv_bytes<D>();
-  constexpr int kQBytes = kHalves * kHalfBytes;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* sK = sQ + kQBytes;
+  uint8_t* sK = base;
   uint8_t* sV = sK + kKStages * kKV;
   PfBars& bar = *reinterpret_cast<PfBars*>(sV + kVStages * kKV);
 
@@ -133,7 +132,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (tile.r < 0) return;  // uniform over the CTA, before any barrier
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_full, 4);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bar.k_full[s], 1);
       mbar_init(&bar.k_empty[s], 2);  // released by both CTAs' S products
@@ -152,7 +151,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     fence_barrier_init();
   }
   if (warp == 4 && lane == 0) {
-    prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
   }
@@ -192,12 +190,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const int ppt = kKeys / box;  // pages per key tile
     const int npages_req = (seq + BS - 1) / BS;
     const int32_t* bt = p.a.block_table + (long long)r * p.a.bt_stride;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar.q_full, (uint32_t)kQBytes);
-#pragma unroll
-      for (int h = 0; h < kHalves; ++h)
-        tma_load_3d(sQ + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G, q_start + tok0);
-    }
     // page ids of key tile j (lane i < ppt: page i of the tile)
     auto tile_pages = [&](int j) -> int {
       const int lp = (kt0 + j) * kKeys / BS + lane;
@@ -262,7 +254,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
       // the copies already issued land before the CTA's shared memory is released
-      mbar_wait(&bar.q_full, 0);
       for (int jj = k_issued > kKStages ? k_issued - kKStages : 0; jj < k_issued; ++jj)
         mbar_wait(&bar.k_full[jj % kKStages], (uint32_t)((jj / kKStages) & 1));
       for (int jj = v_issued > kVStages ? v_issued - kVStages : 0; jj < v_issued; ++jj)
@@ -290,10 +281,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tcgen05_fence_after();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t qa = smem_u32(sQ) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
             const uint32_t ka = smem_u32(sK + s * kKV) + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-            umma_bf16(tmem + sb * kKeys, umma_desc_sw128(qa, 16, 1024),
-                      umma_desc_sw128(ka, 16, 1024), idS, ks > 0);
+            umma_bf16_tmem_a(tmem + sb * kKeys, tmem + kTmemQ + ks * 8,
+                             umma_desc_sw128(ka, 16, 1024), idS, ks > 0);
           }
           umma_commit(&bar.s_full[sb]);
           umma_commit_multicast(&bar.k_empty[s], (uint16_t)0x3);
@@ -339,6 +329,31 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // keys every row of the tile attends: [tile_min_kv_max, tile_max_kv_min]
     const int tile_max_kv_min = min(ctx + tok0, seq - 1);
     const int tile_min_kv_max = W > 0 ? max(0, ctx + tok_end - 1 - W + 1) : 0;
+    // this row's query (one token, one head: head_dim contiguous bf16) into TMEM as
+    // the A operand of S = Q K^T; rows past the step read as zeros
+    {
+      const long long qrow = (long long)q_start + tok;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.a.q) +
+                                                        (qrow * p.a.num_q_heads + g * G + hh) * D);
+      const bool in_step = qrow < p.a.num_tokens;
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 16) {
+        uint32_t qk[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 x = in_step ? __ldg(src + c0 / 4 + v) : make_uint4(0, 0, 0, 0);
+          qk[4 * v + 0] = x.x;
+          qk[4 * v + 1] = x.y;
+          qk[4 * v + 2] = x.z;
+          qk[4 * v + 3] = x.w;
+        }
+        tmem_st16(tmem + lane_addr + kTmemQ + c0, qk);
+      }
+      tmem_wait_st();
+      tcgen05_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.q_full);
+    }
     float m_ref = -FLT_MAX;
     float l = 0.f;
     for (int j = 0; j < nkt; ++j) {
@@ -511,21 +526,16 @@ cudaError_t encode(CUtensorMap* map, void* ptr, int rank, const cuuint64_t* dims
 template <int D>
 cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
   const StepArgs& a = p.a;
-  const int G = a.num_q_heads / a.num_kv_heads;
   const cuuint64_t e = 2;
-  CUtensorMap mq, mk, mv;
-  // q as (d, head, token); box: 64 of d, the G heads of one KV head, the tile's tokens
-  cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
-  cuuint64_t qs[2] = {(cuuint64_t)D * e, (cuuint64_t)a.num_q_heads * D * e};
-  cuuint32_t qb[3] = {64, (cuuint32_t)G, (cuuint32_t)p.tile_tokens};
-  cudaError_t err = encode(&mq, const_cast<void*>(a.q), 3, qd, qs, qb);
+  CUtensorMap mk, mv;
+  cudaError_t err = cudaSuccess;
   // caches as (d, key in page, head, page); box: 64 of d, box_keys keys, one head, one page
   cuuint64_t cd[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size, (cuuint64_t)a.num_kv_heads,
                       (cuuint64_t)a.num_blocks};
   cuuint64_t cs[3] = {(cuuint64_t)a.num_kv_heads * D * e, (cuuint64_t)D * e,
                       (cuuint64_t)a.block_size * a.num_kv_heads * D * e};
   cuuint32_t cb_[4] = {64, (cuuint32_t)p.box_keys, 1, 1};
-  if (err == cudaSuccess) err = encode(&mk, a.k_cache, 4, cd, cs, cb_);
+  err = encode(&mk, a.k_cache, 4, cd, cs, cb_);
   if (err == cudaSuccess) err = encode(&mv, a.v_cache, 4, cd, cs, cb_);
   if (err != cudaSuccess) return err;
   auto kern = prefill_tile_kernel<D>;
@@ -536,15 +546,15 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  return launch_pdl_cluster(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), 2, smem, s, mq,
-                            mk, mv, p);
+  return launch_pdl_cluster(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), 2, smem, s, mk, mv,
+                            p);
 }
 
 }  // namespace
 
 size_t prefill_smem_bytes(int head_dim) {
   const size_t kv = (size_t)(head_dim / 64) * kHalfBytes;
-  size_t b = 1024 + kv /* Q */ + (kKStages + kVStages) * kv + sizeof(PfBars);
+  size_t b = 1024 + (kKStages + kVStages) * kv + sizeof(PfBars);
   // at least ~half the SM's shared memory, so that a second CTA (and a second
   // 512-column TMEM allocation) never lands on the same SM
   if (b < 120 * 1024) b = 120 * 1024;
