@@ -125,7 +125,10 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   }
 
   // ---- prefill rows: tcgen05 tile kernel, heaviest requests first
-  const bool prefill_ok = has_prefill && a.block_size % 8 == 0 && G <= 16 && kRowsPerTile % G == 0;
+  // a 128-key tile is made of whole page boxes (block_size divides 128) or lies
+  // inside one page (block_size a multiple of 128)
+  const bool tile_pages_ok = a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
+  const bool prefill_ok = has_prefill && tile_pages_ok && G <= 16 && kRowsPerTile % G == 0;
   if (prefill_ok) {
     const int TQ = kRowsPerTile / G;
     std::vector<std::pair<long long, int>> order;  // (weight, r)
@@ -142,6 +145,8 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
         pa.tile_tokens = TQ;
         pa.box_keys = std::min(a.block_size, 128);
         pa.n_entries = 0;
+        // the scatter, the decode kernel or an earlier prefill launch runs first
+        pa.metadata_ready = (scatter_first || plan.fast_decode || l > 0) ? 1 : 0;
         pa.total_ctas = 0;
         for (size_t i = (size_t)l * kPrefillMaxEntries;
              i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
@@ -150,7 +155,10 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
           PrefillEntry& e = pa.entries[pa.n_entries++];
           e.r = r;
           e.n_qtiles = (ql + TQ - 1) / TQ;
-          pa.total_ctas += 2 * ((e.n_qtiles + 1) / 2) * a.num_kv_heads;  // clusters of two
+          e.q_start = h_qsl[r];
+          e.q_len = ql;
+          e.seq_len = h_seq_lens[r];
+          pa.total_ctas += prefill_ctas(e.n_qtiles, a.num_kv_heads);
         }
       }
       plan.n_prefill_launches = n_launch;

@@ -166,6 +166,13 @@ CB_DEV uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The address-independent part of a 128B-swizzle descriptor: OR (or add) the
+// shared-memory address >> 4 into the low 14 bits to get umma_desc_sw128(address, ...).
+__host__ __device__ constexpr uint64_t umma_desc_sw128_base(uint32_t lbo, uint32_t sbo) {
+  return ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
 // b_mn_major: B stored with N contiguous (else K contiguous); A is K-major.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major) {
@@ -197,6 +204,38 @@ CB_DEV void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_u32(bar)),
       "h"(cta_mask)
+      : "memory");
+}
+
+// The same three operations for a whole warp in uniform control flow: every lane
+// executes them (so that descriptors stay warp-uniform) and the lane that
+// elect.sync picks issues. All lanes active, the pick is the same lane every
+// time, so these commits track that lane's MMAs.
+CB_DEV void umma_bf16_elect(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 x;\n\telect.sync x|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+CB_DEV void umma_bf16_tmem_a_elect(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 x;\n\telect.sync x|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+CB_DEV void umma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 x;\n\telect.sync x|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 
@@ -286,6 +325,13 @@ CB_DEV float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family)
+CB_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 CB_DEV uint32_t pack_bf16x2(float lo, float hi) {
