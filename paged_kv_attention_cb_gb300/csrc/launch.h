@@ -59,30 +59,6 @@ cudaError_t launch_pdl(KernelId id, void (*kernel)(KArgs...), dim3 grid, dim3 bl
   return e;
 }
 
-// The same with thread-block clusters of `cluster_x` CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(KernelId id, void (*kernel)(KArgs...), dim3 grid, dim3 block,
-                               unsigned cluster_x, size_t smem, cudaStream_t stream,
-                               Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = cluster_x;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  note_launch_begin(id, stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-  note_launch_end(id, stream);
-  return e;
-}
 
 cudaError_t launch_write_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                             const int64_t* slot_mapping, int32_t num_tokens, int64_t num_slots,

@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for sm_100-family features used by the libcb kernels:
 // mbarriers with bounded waits, TMA (tensor and bulk) copies, ldmatrix,
-// movmatrix and the bf16 mma.sync used for the decode contraction.
+// movmatrix and the bf16 mma.sync used for the decode contraction, and the
+// tcgen05 MMA / TMEM operations of the prefill kernel.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -82,38 +83,6 @@ CB_DEV void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       : "memory");
 }
 
-CB_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-// The same tile into the shared memory of every CTA in `cta_mask` (same offset in
-// each), completing bytes on the mbarrier at `bar`'s offset in each of them.
-CB_DEV void tma_load_4d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                  int c1, int c2, int c3, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
-      "r"(c3), "h"(cta_mask)
-      : "memory");
-}
-
-CB_DEV uint32_t cluster_cta_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of all CTAs in the cluster (release / acquire at cluster scope).
-CB_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
 CB_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -154,20 +123,11 @@ CB_DEV void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, u
 
 // ------------------------------------------------------------------ tcgen05 (5th-gen tensor cores)
 
-// Shared-memory matrix descriptor for a 128B-swizzled operand: start address,
-// leading and stride byte offsets (sm_100 layout: version 1, swizzle mode 2).
-CB_DEV uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// The address-independent part of a 128B-swizzle descriptor: OR (or add) the
-// shared-memory address >> 4 into the low 14 bits to get umma_desc_sw128(address, ...).
+// Shared-memory matrix descriptor of a 128B-swizzled operand (sm_100 layout:
+// leading and stride byte offsets >> 4 at bits 16 and 32, version 1 at bit 46,
+// swizzle mode 2 at bit 61), without its start address: OR (or add) the
+// shared-memory start address >> 4 into the low 14 bits. Shared addresses stay
+// below 2^18, so adding offsets >> 4 never carries out of that field.
 __host__ __device__ constexpr uint64_t umma_desc_sw128_base(uint32_t lbo, uint32_t sbo) {
   return ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
@@ -178,33 +138,6 @@ __host__ __device__ constexpr uint64_t umma_desc_sw128_base(uint32_t lbo, uint32
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-CB_DEV void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                      uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
-CB_DEV void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `cta_mask` once every
-// tcgen05.mma issued so far by this thread has completed.
-CB_DEV void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // The same three operations for a whole warp in uniform control flow: every lane
@@ -290,16 +223,6 @@ CB_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 
-// D (TMEM) = A (TMEM: lane = row, 32-bit column = two consecutive K elements) * B (smem).
-CB_DEV void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc, uint32_t idesc,
-                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 CB_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 CB_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -307,16 +230,6 @@ CB_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "
 // (tensor cores, TMA) before it signals them.
 CB_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Warpgroup register reallocation (all four warps of a warpgroup execute it).
-template <uint32_t N>
-CB_DEV void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-CB_DEV void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero; relative
