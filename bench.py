@@ -1,7 +1,7 @@
 """Benchmark one continuous-batching paged-attention step through libcb's C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config decode|mixed|long_decode|long_decode_window|tiny_mixed]
+                    [--config decode|mixed|long_decode|long_decode_window|tiny_mixed|trace]
 
 A step is the whole hot path on one synthetic batch: scatter of the step's new
 K/V through slot_mapping, then paged attention of every query row (decode and
@@ -18,6 +18,12 @@ and leaves L2 clean (``--flush write`` writes 512 MiB instead, which leaves
 dirty lines whose write-back then competes with the step's reads). With N > 1 (torchrun), every rank runs an independent
 replica of the step (the path needs no exchange) and the job value is the sum
 of the bytes over the slowest rank's time.
+
+``--config trace`` replays the FIFO continuous-batching trace (512 requests,
+lognormal prompts, geometric outputs, max_batch_tokens 4096, 65536 pages of 16
+tokens) step by step: every step is scatter + attention of that step's batch,
+timed on its own; the line reports the whole trace's KV GB/s and tokens/s with
+per-step percentiles.
 
 ``--impl reference`` times the CPU oracle (float64 NumPy, as it stands) on the
 same workload instead, on the host cores.
@@ -366,6 +372,235 @@ def oracle_sample_size(config):
             "long_decode_window": 8}.get(config)
 
 
+# ---------------------------------------------------------------- trace (c5)
+
+
+def compact_spec(spec):
+    """The same step over a pool holding only its own pages (renumbered after the
+    reserved ones), so that the oracle can be timed on it without the whole pool."""
+    used = sorted({int(p) for r in range(spec.R)
+                   for p in spec.block_table[r, :-(-int(spec.seq_lens[r]) // spec.block_size)]})
+    remap = {p: workloads.RESERVED_PAGES + i for i, p in enumerate(used)}
+    bt = np.zeros_like(spec.block_table)
+    for r in range(spec.R):
+        n = -(-int(spec.seq_lens[r]) // spec.block_size)
+        bt[r, :n] = [remap[int(p)] for p in spec.block_table[r, :n]]
+    slots = np.array([remap[int(s) // spec.block_size] * spec.block_size + int(s) % spec.block_size
+                      for s in spec.slot_mapping], dtype=np.int64)
+    return workloads.StepSpec(**{**spec.__dict__, "block_table": bt, "slot_mapping": slots,
+                                 "num_blocks": workloads.RESERVED_PAGES + len(used)})
+
+
+def trace_specs(n_steps=0):
+    from workloads.fifo_trace import TraceConfig, fifo_trace
+
+    cfg = TraceConfig()
+    specs = [st.spec for st in fifo_trace(cfg, max_steps=n_steps or None)]
+    return cfg, specs
+
+
+def run_trace_ours(args, cfg, specs, world, rank, local):
+    """Every trace step through the C ABI with the cache carried from step to step."""
+    import torch
+
+    import paged_kv_attention_cb_gb300 as cb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(cfg.seed)
+    shape = (cfg.num_pages, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
+    k_cache = torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+    v_cache = torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+    max_r = max(sp.R for sp in specs)
+    max_t = max(sp.T for sp in specs)
+    ws = cb.alloc_workspace(max_r, max_t, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, dev)
+    out_buf = torch.empty(max_t, cfg.num_q_heads, cfg.head_dim, dtype=torch.bfloat16, device=dev)
+    flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    # every step's inputs drawn once (seed = trace seed + step), resident in HBM
+    steps = []
+    for sp in specs:
+        gs = torch.Generator(device=dev)
+        gs.manual_seed(int(sp.seed))
+        f = lambda *sh: torch.randn(*sh, generator=gs, device=dev).to(torch.bfloat16)
+        q = f(sp.T, sp.num_q_heads, sp.head_dim)
+        kn = f(sp.T, sp.num_kv_heads, sp.head_dim)
+        vn = f(sp.T, sp.num_kv_heads, sp.head_dim)
+        steps.append((sp, q, kn, vn, workloads.metadata_tensors(sp, dev)))
+    torch.cuda.synchronize()
+
+    def call(i, q=None, kn=None, vn=None, md=None):
+        sp, q0, kn0, vn0, md0 = steps[i]
+        md = md or md0
+        cb.paged_attention(out_buf[:sp.T], q0 if q is None else q, k_cache, v_cache,
+                           md["query_start_loc"], md["seq_lens"], md["block_table"],
+                           sp.query_start_loc, sp.seq_lens, ws, scale=sp.scale,
+                           k_new=kn0 if kn is None else kn, v_new=vn0 if vn is None else vn,
+                           slot_mapping=md["slot_mapping"], stream=stream)
+
+    n = len(steps)
+    for i in range(min(args.warmup, n)):
+        call(i)
+    torch.cuda.synchronize()
+    if cb.read_error_word(ws) != 0:
+        raise RuntimeError("device bounds check fired during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    launches0 = cb.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(n):
+            flush_buf.max()  # evicts L2 (clean) between steps
+            ev[i][0].record(stream)
+            call(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = cb.launch_count() - launches0
+    if cb.read_error_word(ws) != 0:
+        raise RuntimeError("device bounds check fired during the trace")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    cb.kernel_timing(True)
+    for i in range(n):
+        flush_buf.max()
+        call(i)
+    per_kernel = cb.kernel_timing_collect()
+    cb.kernel_timing(False)
+
+    # end to end: each step's inputs and metadata from pinned host memory, output back
+    hq = torch.empty(max_t * cfg.num_q_heads * cfg.head_dim, dtype=torch.bfloat16, pin_memory=True)
+    hk = torch.empty(max_t * cfg.num_kv_heads * cfg.head_dim, dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    ho = torch.empty_like(hq, pin_memory=True)
+    dq = torch.empty_like(out_buf)
+    dk = torch.empty(max_t, cfg.num_kv_heads, cfg.head_dim, dtype=torch.bfloat16, device=dev)
+    dvv = torch.empty_like(dk)
+    e2e_ms = 0.0
+    h2d = d2h = 0
+    for i in range(n):
+        sp, q, kn, vn, md = steps[i]
+        nq, nk = q.numel(), kn.numel()
+        hq[:nq].copy_(q.view(-1))
+        hk[:nk].copy_(kn.view(-1))
+        hv[:nk].copy_(vn.view(-1))
+        hmd = {k: v.cpu().pin_memory() for k, v in md.items()}
+        dmd = {k: torch.empty_like(v, device=dev) for k, v in hmd.items()}
+        torch.cuda.synchronize()
+        flush_buf.max()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dq[:sp.T].view(-1).copy_(hq[:nq], non_blocking=True)
+        dk[:sp.T].view(-1).copy_(hk[:nk], non_blocking=True)
+        dvv[:sp.T].view(-1).copy_(hv[:nk], non_blocking=True)
+        for k in dmd:
+            dmd[k].copy_(hmd[k], non_blocking=True)
+        call(i, dq[:sp.T], dk[:sp.T], dvv[:sp.T], dmd)
+        ho[:nq].copy_(out_buf[:sp.T].view(-1), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += a.elapsed_time(b)
+        h2d += 2 * (nq + 2 * nk) + sum(v.numel() * v.element_size() for v in hmd.values())
+        d2h += 2 * nq
+    return dict(step_ms=step_ms, launches=launches, per_kernel=per_kernel, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, clocks=clocks.summary())
+
+
+def trace_oracle(specs, budget_s, max_requests=24):
+    """The oracle (as it stands) on evenly spaced sampled steps, each over its own
+    compacted pool and at most `max_requests` requests, until the budget is spent."""
+    n = len(specs)
+    # coarse to fine over the trace, then its first and last steps
+    ks = [8, 4, 12, 2, 6, 10, 14, 1, 3, 5, 7, 9, 11, 13, 15]
+    order = list(dict.fromkeys([int(k * n / 16) for k in ks] + [0, n - 1]))
+    done_b = done_t = 0
+    el = 0.0
+    used = []
+    for i in order:
+        sample = compact_spec(oracle_sample_spec(specs[i], max_requests)[0])
+        h = oracle_inputs(sample)
+        _, t = time_oracle(sample, 0.0, h, max_steps=1)
+        el += t
+        done_b += kv_bytes(sample)
+        done_t += sample.T
+        used.append(i)
+        if el >= budget_s:
+            break
+    return done_b, done_t, el, used
+
+
+def trace_main(args, world, rank, local, metric):
+    cfg, specs = trace_specs(args.trace_steps)
+    kvb = [kv_bytes(sp) for sp in specs]
+    tot_b, tot_t = sum(kvb), sum(sp.T for sp in specs)
+    conf = {"workload": "fifo_trace_512req_bf16", "requests": cfg.num_requests,
+            "trace_steps": len(specs), "query_tokens": tot_t,
+            "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
+            "head_dim": cfg.head_dim, "block_size": cfg.block_size,
+            "num_blocks": cfg.num_pages, "max_batch_tokens": cfg.max_batch_tokens,
+            "max_requests_per_batch": cfg.max_requests_per_batch,
+            "safety_margin": cfg.safety_margin, "kv_bytes_total": tot_b,
+            "l2": "512 MiB read between timed steps (L2 evicted, clean)",
+            "parallelism": f"replicas x{world}"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        b, t, el, used = trace_oracle(specs, args.cpu_budget)
+        val = b / el / 1e9
+        line = {"impl": "reference", "metric": metric, "value": val, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": len(used), "warmup": 0,
+                "ms_per_step": 1e3 * el / len(used), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": conf, "tokens_per_s": t / el,
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"trace steps {used}, first 24 requests each"},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    res = run_trace_ours(args, cfg, specs, world, rank, local)
+    total_ms = reduce_max(sum(res["step_ms"]), world)
+    if rank != 0:
+        return
+    n = len(specs)
+    value = world * tot_b / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    pk = res["per_kernel"]
+    dom = max(pk.items(), key=lambda kv: kv[1][0])[0] if pk else None
+    dom_ms = pk[dom][0] if dom else None  # summed over all steps
+    dom_bytes = sum(decode_kernel_bytes(sp) for sp in specs) if dom == "decode_split" else None
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if (dom_bytes and dom_ms) else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "algorithmic_bytes_per_launch": (dom_bytes / pk[dom][1]) if dom_bytes else None,
+                "avg_launch_ms": (dom_ms / pk[dom][1]) if dom else None, "traffic": None}
+    step_gbs = [b / (ms * 1e-3) / 1e9 for b, ms in zip(kvb, res["step_ms"])]
+    pct = lambda a, q: float(np.percentile(np.asarray(a), q))
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        b, t, el, used = trace_oracle(specs, args.cpu_budget)
+        cpu = {"value": b / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"trace steps {used} (first 24 requests each), {el:.1f} s"}
+    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": total_ms / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": conf,
+            "tokens_per_s": world * tot_t / (total_ms * 1e-3),
+            "step_ms_percentiles": {q: pct(res["step_ms"], q) for q in (10, 50, 90, 99)},
+            "step_gbs_percentiles": {q: pct(step_gbs, q) for q in (10, 50, 90)},
+            "e2e": {"value": world * tot_b / (res["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": res["e2e_ms"] / n, "h2d_bytes_per_step": res["h2d"] / n,
+                    "d2h_bytes_per_step": res["d2h"] / n},
+            "gpu_launches": res["launches"],
+            "per_kernel_ms": {k: v[0] / v[1] for k, v in pk.items()},
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": res["clocks"]}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -375,7 +610,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="decode", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="decode", choices=sorted(workloads.CONFIGS) + ["trace"])
+    ap.add_argument("--trace-steps", type=int, default=0,
+                    help="--config trace: time only the first N steps of the trace (0: all)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -386,9 +623,12 @@ def main():
         args.warmup = 3
 
     world, rank, local = dist_setup()
+    metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
+    if args.config == "trace":
+        trace_main(args, world, rank, local, metric)
+        return
     spec = workloads.by_name(args.config)
     kvb = kv_bytes(spec)
-    metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
     cfg = {"workload": spec.name, "requests": spec.R, "query_tokens": spec.T,
            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
            "head_dim": spec.head_dim, "block_size": spec.block_size,
