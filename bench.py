@@ -23,7 +23,8 @@ of the bytes over the slowest rank's time.
 lognormal prompts, geometric outputs, max_batch_tokens 4096, 65536 pages of 16
 tokens) step by step: every step is scatter + attention of that step's batch,
 timed on its own; the line reports the whole trace's KV GB/s and tokens/s with
-per-step percentiles.
+per-step percentiles. ``--config trace_prefill_first`` replays the same request
+stream under the prefill-first policy (safety margin 0).
 
 ``--impl reference`` times the CPU oracle (float64 NumPy, as it stands) on the
 same workload instead, on the host cores.
@@ -391,10 +392,10 @@ def compact_spec(spec):
                                  "num_blocks": workloads.RESERVED_PAGES + len(used)})
 
 
-def trace_specs(n_steps=0):
-    from workloads.fifo_trace import TraceConfig, fifo_trace
+def trace_specs(n_steps=0, policy="fifo"):
+    from workloads.fifo_trace import TraceConfig, fifo_trace, prefill_first_config
 
-    cfg = TraceConfig()
+    cfg = TraceConfig() if policy == "fifo" else prefill_first_config()
     specs = [st.spec for st in fifo_trace(cfg, max_steps=n_steps or None)]
     return cfg, specs
 
@@ -533,10 +534,12 @@ def trace_oracle(specs, budget_s, max_requests=24):
 
 
 def trace_main(args, world, rank, local, metric):
-    cfg, specs = trace_specs(args.trace_steps)
+    policy = "prefill_first" if args.config == "trace_prefill_first" else "fifo"
+    cfg, specs = trace_specs(args.trace_steps, policy)
     kvb = [kv_bytes(sp) for sp in specs]
     tot_b, tot_t = sum(kvb), sum(sp.T for sp in specs)
-    conf = {"workload": "fifo_trace_512req_bf16", "requests": cfg.num_requests,
+    conf = {"workload": f"{policy}_trace_512req_bf16", "requests": cfg.num_requests,
+            "policy": policy,
             "trace_steps": len(specs), "query_tokens": tot_t,
             "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
             "head_dim": cfg.head_dim, "block_size": cfg.block_size,
@@ -610,7 +613,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="decode", choices=sorted(workloads.CONFIGS) + ["trace"])
+    ap.add_argument("--config", default="decode",
+                    choices=sorted(workloads.CONFIGS) + ["trace", "trace_prefill_first"])
     ap.add_argument("--trace-steps", type=int, default=0,
                     help="--config trace: time only the first N steps of the trace (0: all)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -624,7 +628,7 @@ def main():
 
     world, rank, local = dist_setup()
     metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
-    if args.config == "trace":
+    if args.config.startswith("trace"):
         trace_main(args, world, rank, local, metric)
         return
     spec = workloads.by_name(args.config)

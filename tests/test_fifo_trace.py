@@ -113,3 +113,58 @@ def test_small_trace_runs_to_completion():
     assert steps and steps[-1].spec.T >= 1
     total_tokens = sum(int(st.spec.T) for st in steps)
     assert total_tokens > 60
+
+
+# ------------------------------------------------------------------ prefill-first policy
+
+
+def test_prefill_first_orders_prefills_before_decodes():
+    from workloads.fifo_trace import prefill_first_config
+
+    cfg = prefill_first_config(max_batch_tokens=64, max_requests_per_batch=16, num_pages=1024)
+    assert cfg.safety_margin == 0.0 and cfg.policy == "prefill_first"
+    reqs = [Request(0, 8, 5, 0), Request(1, 100, 5, 0), Request(2, 10, 5, 1)]
+    s = FifoScheduler(cfg, reqs)
+    b0 = s.schedule()  # request 0 whole, request 1 chunked to the budget
+    assert [(r.rid, c, q) for r, c, q in b0] == [(0, 0, 8), (1, 0, 56)]
+    s.complete(b0)
+    # step 1: request 1's next chunk first, then arrival 2, then the decode of 0
+    b1 = s.schedule()
+    assert [(r.rid, c, q) for r, c, q in b1] == [(1, 56, 44), (2, 0, 10), (0, 8, 1)]
+
+
+def test_prefill_first_decodes_wait_while_prefills_fill_the_budget():
+    from workloads.fifo_trace import prefill_first_config
+
+    cfg = prefill_first_config(max_batch_tokens=32, num_pages=1024)
+    s = FifoScheduler(cfg, [Request(0, 4, 10, 0), Request(1, 200, 3, 1)])
+    s.complete(s.schedule())  # request 0's prompt, which yields its first token
+    b = s.schedule()          # request 1 arrives: its chunk takes the whole budget
+    assert [(r.rid, q) for r, _, q in b] == [(1, 32)]
+    # FIFO on the same stream decodes request 0 first
+    f = FifoScheduler(TraceConfig(max_batch_tokens=32, num_pages=1024, safety_margin=0.0),
+                      [Request(0, 4, 10, 0), Request(1, 200, 3, 1)])
+    f.complete(f.schedule())
+    assert [(r.rid, q) for r, _, q in f.schedule()] == [(0, 1), (1, 31)]
+
+
+def test_prefill_first_trace_runs_to_completion():
+    from workloads.fifo_trace import prefill_first_config
+
+    cfg = prefill_first_config(num_requests=60, prompt_median=100, output_mean=20,
+                               arrivals_per_step=8, max_batch_tokens=512,
+                               max_requests_per_batch=32, num_pages=600)
+    n_steps = n_mixed = total = 0
+    for st in fifo_trace(cfg):  # inspected before the step completes: states as scheduled
+        sp = st.spec
+        assert sp.T <= cfg.max_batch_tokens and sp.R <= cfg.max_requests_per_batch
+        kinds = [r.state for r, _, _ in st.entries]
+        if "DECODING" in kinds and "PREFILLING" in kinds:
+            n_mixed += 1
+            last_prefill = max(i for i, k in enumerate(kinds) if k == "PREFILLING")
+            first_decode = min(i for i, k in enumerate(kinds) if k == "DECODING")
+            assert last_prefill < first_decode
+        n_steps += 1
+        total += int(sp.T)
+    # prefills take the whole budget most steps, so few steps mix the two kinds
+    assert n_steps > 20 and n_mixed >= 1 and total > 60

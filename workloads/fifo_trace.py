@@ -22,8 +22,14 @@ request stream into the per-step metadata the attention step consumes
   active request is never reset (sections "Soft reset", "Offloading");
 * finished requests free their pages at once; pages 0-1 are reserved.
 
+The second policy, prefill-first (section "PrefillFirst"), finishes chunked
+prefills before it resumes decoding: active prefills first, then waiting
+requests, then decodes with the budget that is left; its safety margin
+defaults to 0 (section "Admission").
+
 Readings (the pages leave them open): arrivals are drawn per step; a soft-reset
-request re-enters at the head of the waiting queue.
+request re-enters at the head of the waiting queue; prefill-first still gives
+decodes whatever token and request budget the prefills leave.
 """
 from __future__ import annotations
 
@@ -55,6 +61,13 @@ class TraceConfig:
     head_dim: int = 128
     dtype: str = "bf16"
     seed: int = 4
+    policy: str = "fifo"        # "fifo" or "prefill_first"
+
+
+def prefill_first_config(**kw) -> TraceConfig:
+    """The prefill-first trace: same request stream, safety margin 0."""
+    kw.setdefault("safety_margin", 0.0)
+    return TraceConfig(policy="prefill_first", **kw)
 
 
 @dataclasses.dataclass
@@ -175,8 +188,8 @@ class FifoScheduler:
             tokens += q_len
             return True
 
-        # 1. decodes, 2. active prefills (FIFO over the active set)
-        for kind in ("DECODING", "PREFILLING"):
+        def active_of(kind):
+            # FIFO over the active set
             for req in list(self.active):
                 if req.state != kind or req not in self.active:
                     continue
@@ -187,19 +200,30 @@ class FifoScheduler:
                 else:
                     n = min(req.prompt_len - req.prefilled, cfg.max_batch_tokens - tokens)
                     fit(req, req.prefilled, n)
-        # 3. waiting requests in arrival order, while the pool keeps its safety margin
-        while (self.waiting and len(batch) < cfg.max_requests_per_batch
-               and tokens < cfg.max_batch_tokens):
-            if self.pool.available() < cfg.safety_margin * self.pool.capacity:
-                break
-            req = self.waiting[0]
-            n = min(req.prompt_len, cfg.max_batch_tokens - tokens)
-            if self._pages_needed(req, n) > self.pool.available():
-                break  # admission needs every page of the first chunk
-            self.waiting.popleft()
-            req.state = "PREFILLING"
-            self.active.append(req)
-            fit(req, 0, n)
+
+        def admit():
+            # waiting requests in arrival order, while the pool keeps its safety margin
+            while (self.waiting and len(batch) < cfg.max_requests_per_batch
+                   and tokens < cfg.max_batch_tokens):
+                if self.pool.available() < cfg.safety_margin * self.pool.capacity:
+                    break
+                req = self.waiting[0]
+                n = min(req.prompt_len, cfg.max_batch_tokens - tokens)
+                if self._pages_needed(req, n) > self.pool.available():
+                    break  # admission needs every page of the first chunk
+                self.waiting.popleft()
+                req.state = "PREFILLING"
+                self.active.append(req)
+                fit(req, 0, n)
+
+        if cfg.policy == "prefill_first":
+            active_of("PREFILLING")
+            admit()
+            active_of("DECODING")
+        else:
+            active_of("DECODING")
+            active_of("PREFILLING")
+            admit()
         return batch
 
     def complete(self, batch):
