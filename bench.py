@@ -24,7 +24,9 @@ lognormal prompts, geometric outputs, max_batch_tokens 4096, 65536 pages of 16
 tokens) step by step: every step is scatter + attention of that step's batch,
 timed on its own; the line reports the whole trace's KV GB/s and tokens/s with
 per-step percentiles. ``--config trace_prefill_first`` replays the same request
-stream under the prefill-first policy (safety margin 0).
+stream under the prefill-first policy (safety margin 0). ``--config copy_blocks``
+times the batched block copy behind swapping (8192 blocks of 32 KB for K and V
+between disjoint pool blocks; bytes read + written).
 
 ``--impl reference`` times the CPU oracle (float64 NumPy, as it stands) on the
 same workload instead, on the host cores.
@@ -604,6 +606,141 @@ def trace_main(args, world, rank, local, metric):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- block copy (swap data movement)
+
+
+COPY_BLOCKS = 8192
+
+
+def copy_main(args, world, rank, local):
+    """Batched block copy: COPY_BLOCKS pairs of disjoint blocks of a 16-token, 8-head,
+    head_dim-128 bf16 pool (K and V); value = bytes read + written / device time."""
+    import torch
+
+    import paged_kv_attention_cb_gb300 as cb
+
+    metric = "batched KV block copy: HBM GB/s (bytes read + written); % of copy roofline"
+    nb, bs, hkv, d = 3 * COPY_BLOCKS, 16, 8, 128
+    block_bytes = bs * hkv * d * 2
+    moved = 2 * 2 * COPY_BLOCKS * block_bytes  # K and V, read and written
+    conf = {"workload": f"copy_{COPY_BLOCKS}_blocks_bf16", "blocks": COPY_BLOCKS,
+            "block_size": bs, "num_kv_heads": hkv, "head_dim": d, "num_blocks": nb,
+            "bytes_per_step": moved, "l2": "512 MiB read between timed steps (L2 evicted, clean)",
+            "parallelism": f"replicas x{world}"}
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(nb).astype(np.int32)
+    src, dst = perm[:COPY_BLOCKS], perm[COPY_BLOCKS:2 * COPY_BLOCKS]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+
+        n = 512  # bounded sample of the same copy
+        hk = np.zeros((n * 3, bs, hkv, d), np.float32)
+        hv = np.zeros_like(hk)
+        per = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.copy_blocks(hk, hv, hk, hv, np.arange(n), np.arange(n, 2 * n))
+            per.append(time.perf_counter() - t0)
+        val = 2 * 2 * n * block_bytes * args.steps / sum(per) / 1e9
+        line = {"impl": "reference", "metric": metric, "value": val, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": 0,
+                "ms_per_step": 1e3 * sum(per) / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": conf,
+                "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"{n} blocks per step (bf16 block bytes counted)"},
+                "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    k = torch.randn(nb, bs, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(nb, bs, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    ds, dd = torch.from_numpy(src).to(dev), torch.from_numpy(dst).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup):
+        cb.copy_blocks(k, v, k, v, ds, dd, error_word=err, stream=stream)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("device bounds check fired")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    launches0 = cb.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for a, b in ev:
+            flush_buf.max()
+            a.record(stream)
+            cb.copy_blocks(k, v, k, v, ds, dd, error_word=err, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = cb.launch_count() - launches0
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), world) / args.steps
+    # end to end: swap-out of the same blocks = gather into staging + copy to pinned host
+    stage_k = torch.empty(COPY_BLOCKS, bs, hkv, d, dtype=torch.bfloat16, device=dev)
+    stage_v = torch.empty_like(stage_k)
+    host_k = torch.empty(stage_k.shape, dtype=torch.bfloat16, pin_memory=True)
+    host_v = torch.empty_like(host_k, pin_memory=True)
+    ids = torch.arange(COPY_BLOCKS, dtype=torch.int32, device=dev)
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush_buf.max()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cb.copy_blocks(k, v, stage_k, stage_v, ds, ids, stream=stream)
+        host_k.copy_(stage_k, non_blocking=True)
+        host_v.copy_(stage_v, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += a.elapsed_time(b)
+    e2e_ms = reduce_max(e2e_ms, world) / args.steps
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    value = world * moved / (ms * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        n = 512
+        hk = np.zeros((n * 3, bs, hkv, d), np.float32)
+        hv = np.zeros_like(hk)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < min(args.cpu_budget, 5.0):
+            oracle.copy_blocks(hk, hv, hk, hv, np.arange(n), np.arange(n, 2 * n))
+            reps += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": 2 * 2 * n * block_bytes * reps / el / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{reps} x {n} blocks (bf16 block bytes counted)"}
+    swapped = 2 * COPY_BLOCKS * block_bytes
+    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": conf,
+            "e2e": {"value": world * swapped / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "what": "swap-out: gather + copy to pinned host, "
+                    "bytes swapped out / time", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": swapped},
+            "gpu_launches": launches,
+            "roofline": {"kernel": "copy_blocks", "bound": "hbm", "achieved": value / world,
+                         "peak": peak, "unit": "GB/s", "frac": value / world / peak,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": moved, "avg_launch_ms": ms,
+                         "traffic": None},
+            "cpu_baseline": cpu, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- main
 
 
@@ -614,7 +751,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode",
-                    choices=sorted(workloads.CONFIGS) + ["trace", "trace_prefill_first"])
+                    choices=sorted(workloads.CONFIGS) + ["trace", "trace_prefill_first",
+                                                         "copy_blocks"])
     ap.add_argument("--trace-steps", type=int, default=0,
                     help="--config trace: time only the first N steps of the trace (0: all)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -630,6 +768,9 @@ def main():
     metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
     if args.config.startswith("trace"):
         trace_main(args, world, rank, local, metric)
+        return
+    if args.config == "copy_blocks":
+        copy_main(args, world, rank, local)
         return
     spec = workloads.by_name(args.config)
     kvb = kv_bytes(spec)

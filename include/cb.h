@@ -105,6 +105,34 @@ cb_status cb_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
                       int32_t* error_word, void* stream);
 
 /*
+ * cb_copy_blocks -- batched copy of whole KV blocks: for every i < n, block
+ * dst_ids[i] of (k_dst, v_dst) becomes block src_ids[i] of (k_src, v_src).
+ *
+ * The data movement of preemption by swapping and of CPU offloading: a request's
+ * blocks are copied out to CPU memory and back into free pool blocks when it
+ * resumes ("Continuous batching mechanics", d9bl.com, section "Running out of KV
+ * cache memory"); the manager batches every offloaded request into one transfer
+ * to a pinned CPU buffer ("Continuous batching architecture", Transformers docs,
+ * section "Offloading"). The usual pattern: gather the blocks into a contiguous
+ * device staging buffer with this call (dst_ids = 0 .. n-1), then one
+ * cudaMemcpyAsync of the staging buffer to pinned host memory; the reverse on
+ * resume. A bit-exact copy.
+ *
+ * k_src, v_src: device [src_num_blocks, block_size, Hkv, D]; k_dst, v_dst: device
+ * [dst_num_blocks, block_size, Hkv, D] (written); src_ids, dst_ids: device int32
+ * [n]. The source and destination may be the same buffers, provided no block is
+ * both a source and a destination of the call; two pairs with the same
+ * destination race (which one wins is unspecified). error_word: optional device
+ * int32 (NULL: no record) that gets CB_DEVERR_BLOCK_ID or-ed in for a pair with an
+ * id out of range (that pair is skipped). Runs asynchronously on `stream`.
+ */
+cb_status cb_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                         int64_t src_num_blocks, int64_t dst_num_blocks, const int32_t* src_ids,
+                         const int32_t* dst_ids, int32_t n, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                         int32_t* error_word, void* stream);
+
+/*
  * cb_workspace_size -- bytes of device workspace cb_paged_attention needs for
  * a step with these sizes (an upper bound; it does not depend on the lengths).
  * The workspace holds the device error word, per-request arrival counters and

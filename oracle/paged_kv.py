@@ -65,6 +65,17 @@ def scatter_kv(k_cache, v_cache, k_new, v_new, slot_mapping):
 # ----------------------------------------------------------- index mapping
 
 
+def copy_blocks(k_dst, v_dst, k_src, v_src, src_ids, dst_ids):
+    """Block ``dst_ids[i]`` of the destination caches becomes block ``src_ids[i]`` of the
+    source caches (in place, pair by pair in order): the copy behind swapping a
+    request's blocks out to CPU memory and back ("Continuous batching mechanics",
+    d9bl.com, section "Running out of KV cache memory"; "Continuous batching
+    architecture", section "Offloading")."""
+    for s, d in zip(np.asarray(src_ids).tolist(), np.asarray(dst_ids).tolist()):
+        k_dst[int(d)] = k_src[int(s)]
+        v_dst[int(d)] = v_src[int(s)]
+
+
 def resolve(block_table_row, kv_pos, block_size):
     """Logical position -> (physical block, offset in block)."""
     return int(block_table_row[kv_pos // block_size]), kv_pos % block_size

@@ -17,6 +17,9 @@ from .build import LIB_PATH
 CB_F32 = 0
 CB_BF16 = 1
 CB_FLAG_PORTABLE_ONLY = 0x1
+CB_DEVERR_BLOCK_ID = 0x1
+CB_DEVERR_SLOT = 0x2
+CB_DEVERR_TIMEOUT = 0x4
 
 STATUS = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_METADATA", 3: "CB_ERR_UNSUPPORTED",
           4: "CB_ERR_WORKSPACE", 5: "CB_ERR_CUDA", 6: "CB_ERR_DEVICE_CHECK"}
@@ -39,6 +42,8 @@ _SIGNATURES = {
     "cb_abi_version": (ctypes.c_int, []),
     "cb_write_kv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _vp, _vp]),
+    "cb_copy_blocks": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64, _vp,
+                                      _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "cb_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "cb_workspace_init": (ctypes.c_int, [_vp, ctypes.c_size_t, _vp]),
     "cb_paged_attention": (ctypes.c_int, [
@@ -126,6 +131,17 @@ def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, error_word=None, stre
     _check(lib().cb_write_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                              _ptr(slot_mapping), T, NB, BS, Hkv, D, _dtype_code(k_new),
                              _ptr(error_word), _stream(stream)))
+
+
+def copy_blocks(k_src, v_src, k_dst, v_dst, src_ids, dst_ids, error_word=None, stream=None):
+    """Block dst_ids[i] of k_dst/v_dst [NBd, BS, Hkv, D] = block src_ids[i] of k_src/v_src."""
+    NBs, BS, Hkv, D = k_src.shape
+    n = int(src_ids.numel())
+    if int(dst_ids.numel()) != n or tuple(k_dst.shape[1:]) != (BS, Hkv, D):
+        raise ValueError("copy_blocks: id counts or block shapes differ")
+    _check(lib().cb_copy_blocks(_ptr(k_src), _ptr(v_src), _ptr(k_dst), _ptr(v_dst), NBs,
+                                k_dst.shape[0], _ptr(src_ids), _ptr(dst_ids), n, BS, Hkv, D,
+                                _dtype_code(k_src), _ptr(error_word), _stream(stream)))
 
 
 def workspace_size(num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim) -> int:

@@ -92,6 +92,32 @@ cb_status cb_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
   return CB_OK;
 }
 
+cb_status cb_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                         int64_t src_num_blocks, int64_t dst_num_blocks, const int32_t* src_ids,
+                         const int32_t* dst_ids, int32_t n, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t dtype,
+                         int32_t* error_word, void* stream) {
+  int elt = 0;
+  cb_status st = check_dtype(dtype, &elt);
+  if (st != CB_OK) return st;
+  if (n < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0)
+    return fail(CB_ERR_INVALID_ARG, "sizes must be positive (n >= 0)");
+  const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_dim * elt;
+  if (block_bytes % 16 != 0 || block_bytes / 16 > (int64_t)1 << 30)
+    return fail(CB_ERR_UNSUPPORTED, "block_size * Hkv * head_dim * element size must be a multiple of 16 bytes");
+  if (n == 0) return CB_OK;
+  if (!k_src || !v_src || !k_dst || !v_dst || !src_ids || !dst_ids)
+    return fail(CB_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst))
+    return fail(CB_ERR_INVALID_ARG, "K/V pointers must be 16-byte aligned");
+  cudaError_t e = cb::launch_copy_blocks(k_src, v_src, k_dst, v_dst, src_ids, dst_ids, n,
+                                         src_num_blocks, dst_num_blocks, block_bytes, error_word,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return CB_OK;
+}
+
 size_t cb_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim) {
   return cb::workspace_bytes(num_requests, num_tokens, num_q_heads, num_kv_heads, head_dim);

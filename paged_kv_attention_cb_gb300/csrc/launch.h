@@ -32,7 +32,8 @@ enum KernelId {
   kPortableAttention = 1,
   kDecodeSplit = 2,
   kPrefillTc = 3,
-  kNumKernels = 4
+  kCopyBlocks = 4,
+  kNumKernels = 5
 };
 
 void note_launch_begin(KernelId id, cudaStream_t stream);
@@ -63,6 +64,12 @@ cudaError_t launch_pdl(KernelId id, void (*kernel)(KArgs...), dim3 grid, dim3 bl
 cudaError_t launch_write_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                             const int64_t* slot_mapping, int32_t num_tokens, int64_t num_slots,
                             int32_t row_bytes, int32_t* error_word, cudaStream_t stream);
+
+// Block k_dst/v_dst[dst_ids[i]] = block k_src/v_src[src_ids[i]] for i < n (device ids).
+cudaError_t launch_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                               const int32_t* src_ids, const int32_t* dst_ids, int32_t n,
+                               int64_t src_blocks, int64_t dst_blocks, int64_t block_bytes,
+                               int32_t* error_word, cudaStream_t stream);
 
 // Portable CUDA-core attention over the query rows of the requests listed in
 // `rows_of` (all rows when mode == 0, only rows of requests with q_len == 1

@@ -43,11 +43,12 @@ def place_logical(cache, block_table_row, values, block_size):
     flat[slots] = values
 
 
-def make_case(q_lens, ctx_lens, Hq, Hkv, D, BS, seed, scale=None, window=0, q_scale=1.0):
+def make_case(q_lens, ctx_lens, Hq, Hkv, D, BS, seed, scale=None, window=0, q_scale=1.0,
+              num_blocks=None):
     """Random step with per-request logical KV kept aside for the brute force."""
     spec = workloads.custom(q_lens, ctx_lens, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                             block_size=BS, dtype="f32", seed=seed, scale=scale,
-                            sliding_window=window)
+                            sliding_window=window, num_blocks=num_blocks)
     rng = np.random.default_rng(seed + 99)
     T = spec.T
     q = rng.standard_normal((T, Hq, D)) * q_scale
@@ -431,3 +432,89 @@ def test_generators_are_seeded_and_consistent():
     assert d.R == 64 and d.T == 64 and 128 <= d.seq_lens.min() and d.seq_lens.max() <= 2048
     m = workloads.mixed_step()
     assert m.T == 2048 and list(m.q_lens[-2:]) == [960, 960] and list(m.ctx_lens[-2:]) == [0, 3072]
+
+
+# ------------------------------------------------------------------ block copy and aliasing
+
+
+def _free_pages(spec):
+    used = {int(p) for r in range(spec.R)
+            for p in spec.block_table[r, :-(-int(spec.seq_lens[r]) // spec.block_size)]}
+    return [p for p in range(workloads.RESERVED_PAGES, spec.num_blocks) if p not in used]
+
+
+def test_copy_blocks_swap_roundtrip_restores_the_request():
+    """Swap a request's context pages out to a staging buffer, clobber them, swap them in
+    to other free pages: its KV read through the new block table is the old KV bit for
+    bit, and the step's output is unchanged."""
+    spec, x = make_case([1, 4, 1], [9, 6, 13], 4, 2, 8, 2, seed=123, num_blocks=48)
+    out0, _, _ = run_oracle(spec, x)
+    r = 2
+    n = -(-int(spec.ctx_lens[r]) // spec.block_size)  # pages that hold context
+    pages = spec.block_table[r, :n].copy()
+    kc, vc = x["k_cache"].copy(), x["v_cache"].copy()
+    before_k = opa.gather_request_kv(kc, spec.block_table[r], int(spec.ctx_lens[r]), spec.block_size)
+    before_v = opa.gather_request_kv(vc, spec.block_table[r], int(spec.ctx_lens[r]), spec.block_size)
+    sk = np.zeros((n,) + kc.shape[1:])
+    sv = np.zeros_like(sk)
+    oracle.copy_blocks(sk, sv, kc, vc, pages, np.arange(n))          # swap out
+    rng = np.random.default_rng(5)
+    kc[pages] = rng.standard_normal(kc[pages].shape)                 # pages reused by others
+    vc[pages] = rng.standard_normal(vc[pages].shape)
+    new_pages = np.array(_free_pages(spec)[:n], dtype=np.int32)
+    assert len(new_pages) == n
+    oracle.copy_blocks(kc, vc, sk, sv, np.arange(n), new_pages)      # swap in elsewhere
+    bt = spec.block_table.copy()
+    bt[r, :n] = new_pages
+    after_k = opa.gather_request_kv(kc, bt[r], int(spec.ctx_lens[r]), spec.block_size)
+    after_v = opa.gather_request_kv(vc, bt[r], int(spec.ctx_lens[r]), spec.block_size)
+    assert np.array_equal(after_k, before_k) and np.array_equal(after_v, before_v)
+    # the step's own tokens land where the new table says
+    slots = spec.slot_mapping.copy()
+    t0 = int(spec.query_start_loc[r])
+    for i in range(int(spec.q_lens[r])):
+        p = int(spec.ctx_lens[r]) + i
+        slots[t0 + i] = int(bt[r, p // spec.block_size]) * spec.block_size + p % spec.block_size
+    out1, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], slots, spec.query_start_loc,
+                             spec.seq_lens, bt, spec.block_size, spec.scale)
+    assert np.array_equal(out0, out1)
+
+
+def test_copy_blocks_moves_k_and_v_and_nothing_else():
+    rng = np.random.default_rng(8)
+    k = rng.standard_normal((12, 2, 1, 4))
+    v = rng.standard_normal((12, 2, 1, 4))
+    k0, v0 = k.copy(), v.copy()
+    src, dst = np.array([3, 7, 5]), np.array([9, 2, 11])
+    oracle.copy_blocks(k, v, k, v, src, dst)
+    for s, d in zip(src, dst):
+        assert np.array_equal(k[d], k0[s]) and np.array_equal(v[d], v0[s])
+    keep = [b for b in range(12) if b not in set(dst.tolist())]
+    assert np.array_equal(k[keep], k0[keep]) and np.array_equal(v[keep], v0[keep])
+
+
+def test_shared_prefix_pages_equal_private_copies():
+    """Two requests whose block tables name the same physical prefix pages get exactly
+    the output they get when each owns a private copy of those pages."""
+    spec, x = make_case([1, 3], [8, 8], 4, 2, 8, 4, seed=31)
+    shared = 2  # the first two pages (8 tokens) of request 0 serve request 1's prefix too
+    kc, vc = x["k_cache"].copy(), x["v_cache"].copy()
+    bt_private = spec.block_table.copy()
+    # private layout: request 1's prefix pages hold a copy of request 0's
+    oracle.copy_blocks(kc, vc, kc, vc, bt_private[0, :shared], bt_private[1, :shared])
+    out_private, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], spec.slot_mapping,
+                                    spec.query_start_loc, spec.seq_lens, bt_private,
+                                    spec.block_size, spec.scale)
+    bt_shared = spec.block_table.copy()
+    bt_shared[1, :shared] = bt_shared[0, :shared]
+    out_shared, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], spec.slot_mapping,
+                                   spec.query_start_loc, spec.seq_lens, bt_shared,
+                                   spec.block_size, spec.scale)
+    assert np.array_equal(out_private, out_shared)
+    # and the shared prefix really is what request 1 attends: against a wrong prefix it differs
+    kc[bt_private[1, 0]] += 1.0
+    out_wrong, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], spec.slot_mapping,
+                                  spec.query_start_loc, spec.seq_lens, bt_private,
+                                  spec.block_size, spec.scale)
+    t1 = int(spec.query_start_loc[1])
+    assert not np.array_equal(out_wrong[t1:], out_shared[t1:])

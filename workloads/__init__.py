@@ -139,6 +139,21 @@ def custom(q_lens, ctx_lens, *, num_q_heads=32, num_kv_heads=8, head_dim=128, bl
                     scale=float(scale), sliding_window=int(sliding_window), seed=seed, q_std=q_std)
 
 
+def share_prefix_pages(spec: StepSpec, donor: int, recipient: int, n_pages: int) -> StepSpec:
+    """The same step with request ``recipient``'s first ``n_pages`` block-table entries
+    pointing at request ``donor``'s first pages: a shared prompt prefix held once in the
+    pool ("Continuous batching architecture", section "Prefix caching": full blocks
+    shared between requests with the same prefix). Only full context blocks of both
+    requests may be shared, so no new token of the step is written into a shared page."""
+    bs = spec.block_size
+    if n_pages * bs > min(int(spec.ctx_lens[donor]), int(spec.ctx_lens[recipient])):
+        raise ValueError("only full context blocks can be shared")
+    bt = spec.block_table.copy()
+    bt[recipient, :n_pages] = bt[donor, :n_pages]
+    return StepSpec(**{**spec.__dict__, "block_table": bt,
+                       "name": f"{spec.name}_shared{donor}to{recipient}x{n_pages}"})
+
+
 def tiny_mixed(seed: int = 0) -> StepSpec:
     """Tiny mixed step, fp32: prefill (4,0), prefill (2,0), chunk (3, ctx 5), decode (1, ctx 8).
 
