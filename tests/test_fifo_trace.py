@@ -168,3 +168,89 @@ def test_prefill_first_trace_runs_to_completion():
         total += int(sp.T)
     # prefills take the whole budget most steps, so few steps mix the two kinds
     assert n_steps > 20 and n_mixed >= 1 and total > 60
+
+
+# ------------------------------------------------------------------ prefix caching
+
+
+def _prefixed(rid, group, prefix_len, own, out, arrival):
+    r = Request(rid, prefix_len + own, out, arrival)
+    r.group, r.prefix_len = group, prefix_len
+    return r
+
+
+def test_prefix_blocks_are_shared_after_they_are_written():
+    cfg = TraceConfig(block_size=16, max_batch_tokens=4096, num_pages=64, safety_margin=0.0)
+    a = _prefixed(0, 0, 64, 10, 5, 0)   # 74-token prompt, 4 full prefix blocks
+    b = _prefixed(1, 0, 64, 30, 5, 0)   # same prefix, arrives with a: nothing cached yet
+    c = _prefixed(2, 0, 64, 3, 5, 1)    # arrives after a's prompt is in the cache
+    s = FifoScheduler(cfg, [a, b, c])
+    b0 = s.schedule()
+    assert [(r.rid, ctx, q) for r, ctx, q in b0] == [(0, 0, 74), (1, 0, 94)]
+    s.complete(b0)
+    b1 = s.schedule()
+    entries = {r.rid: (ctx, q) for r, ctx, q in b1}
+    assert entries[2] == (64, 3)                # c computes only its own 3 tokens
+    assert c.pages[:4] == a.pages[:4]           # the same physical pages
+    assert all(s.pool.ref[p] == 2 for p in a.pages[:4])  # a and c (b registered none: a won)
+    sp = to_spec(cfg, b1, 1)
+    # no slot of the step falls into a shared page
+    shared = set(a.pages[:4])
+    assert not any(int(x) // 16 in shared for x in sp.slot_mapping)
+
+
+def test_shared_pages_return_only_with_their_last_user_and_stay_cached():
+    cfg = TraceConfig(block_size=16, max_batch_tokens=4096, num_pages=40, safety_margin=0.0)
+    a = _prefixed(0, 3, 32, 1, 2, 0)
+    s = FifoScheduler(cfg, [a])
+    while not s.done():
+        s.complete(s.schedule())
+    # a finished: its two prefix pages are free but keep their keys (initialized)
+    assert s.pool.available() == s.pool.capacity and len(s.pool.cached) == 2
+    b = _prefixed(1, 3, 32, 5, 2, s.step_index)
+    s.pending.append(b)
+    s.complete(s.schedule())
+    assert b.reused_tokens == 32 and b.pages[:2] == [s.pool.page_of[(3, 0)], s.pool.page_of[(3, 1)]]
+
+
+def test_initialized_pages_are_demoted_when_uninitialized_run_out():
+    cfg = TraceConfig(block_size=16, max_batch_tokens=4096, num_pages=2 + 6, safety_margin=0.0)
+    a = _prefixed(0, 1, 64, 1, 1, 0)  # 65 tokens: 5 pages, 4 of them prefix blocks
+    s = FifoScheduler(cfg, [a])
+    while not s.done():
+        s.complete(s.schedule())
+    assert len(s.pool.cached) == 4 and len(s.pool.free) == 2
+    got = s.pool.take(3)  # two uninitialized, then the most recently freed initialized
+    assert len(got) == 3 and len(s.pool.cached) == 3
+    assert all(p not in s.pool.key_of for p in got)
+
+
+def test_trace_with_prefix_groups_shares_and_stays_consistent():
+    from workloads.fifo_trace import draw_requests
+
+    cfg = TraceConfig(num_requests=80, prompt_median=60, output_mean=12, arrivals_per_step=6,
+                      max_batch_tokens=1024, max_requests_per_batch=48, num_pages=900,
+                      prefix_groups=3, prefix_len_min=32, prefix_len_max=160, seed=5)
+    s = FifoScheduler(cfg, draw_requests(cfg, np.random.default_rng(cfg.seed)))
+    n_shared_steps = 0
+    while not s.done():
+        batch = s.schedule()
+        sp = to_spec(cfg, batch, s.step_index)
+        owners = {}
+        for r in range(sp.R):
+            n = -(-int(sp.seq_lens[r]) // cfg.block_size)
+            row = sp.block_table[r, :n]
+            assert row.min() >= RESERVED_PAGES
+            for p in row:
+                owners.setdefault(int(p), []).append(r)
+        shared = {p for p, rs in owners.items() if len(rs) > 1}
+        n_shared_steps += bool(shared)
+        # a page in several block tables is a registered prefix block with that many users
+        for p in shared:
+            assert p in s.pool.key_of and s.pool.ref[p] >= len(owners[p])
+        # and the step writes none of them
+        assert not any(int(x) // cfg.block_size in shared for x in sp.slot_mapping)
+        s.complete(batch)
+    assert n_shared_steps > 5
+    assert sum(r.reused_tokens for r in s.finished) > 0
+    assert s.pool.available() == s.pool.capacity  # every reference returned

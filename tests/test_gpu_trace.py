@@ -20,14 +20,17 @@ def draw_step(spec, device="cuda"):
     return f(T, Hq, D), f(T, Hkv, D), f(T, Hkv, D)
 
 
-@pytest.mark.parametrize("policy", ["fifo", "prefill_first"])
+@pytest.mark.parametrize("policy", ["fifo", "prefill_first", "fifo_prefix_cache"])
 def test_reduced_trace_all_steps(policy):
     # the trace's structure (chunked prefills next to decodes, admission under a safety
     # margin, soft resets when the pool runs out) at a size the oracle follows step by step
     kw = dict(num_requests=48, prompt_median=160, prompt_max=1500, output_mean=24,
               arrivals_per_step=6, max_batch_tokens=512, max_requests_per_batch=24,
               num_pages=420, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=4)
-    cfg = TraceConfig(**kw) if policy == "fifo" else prefill_first_config(**kw)
+    if policy == "fifo_prefix_cache":
+        # three shared prompt prefixes: later requests alias the cached prefix pages
+        kw.update(prefix_groups=3, prefix_len_min=32, prefix_len_max=200)
+    cfg = prefill_first_config(**kw) if policy == "prefill_first" else TraceConfig(**kw)
     g = torch.Generator(device="cuda")
     g.manual_seed(4)
     shape = (cfg.num_pages, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
@@ -37,7 +40,7 @@ def test_reduced_trace_all_steps(policy):
     hv = v_cache.float().cpu().numpy()
     ws = cb.alloc_workspace(cfg.max_requests_per_batch, cfg.max_batch_tokens, cfg.num_q_heads,
                             cfg.num_kv_heads, cfg.head_dim)
-    n_steps = n_mixed = 0
+    n_steps = n_mixed = n_aliased = 0
     worst = 0.0
     for st in fifo_trace(cfg):
         sp = st.spec
@@ -61,7 +64,11 @@ def test_reduced_trace_all_steps(policy):
         worst = max(worst, float(err.max()))
         n_steps += 1
         n_mixed += int((sp.q_lens == 1).any() and (sp.q_lens > 1).any())
+        rows = [sp.block_table[r, :-(-int(sp.seq_lens[r]) // sp.block_size)] for r in range(sp.R)]
+        n_aliased += int(len(np.concatenate(rows)) > len(np.unique(np.concatenate(rows))))
     assert cb.read_error_word(ws) == 0
     # the GPU cache after the whole trace equals the oracle's, bit for bit (pages >= 2)
     assert np.array_equal(k_cache.float().cpu().numpy()[2:], hk[2:])
-    assert n_steps > 20 and n_mixed >= (5 if policy == "fifo" else 1)
+    assert n_steps > 20 and n_mixed >= (1 if policy == "prefill_first" else 5)
+    if policy == "fifo_prefix_cache":
+        assert n_aliased > 5

@@ -21,6 +21,14 @@ request stream into the per-step metadata the attention step consumes
   pages are freed and it goes back to the front of the waiting queue; the last
   active request is never reset (sections "Soft reset", "Offloading");
 * finished requests free their pages at once; pages 0-1 are reserved.
+* prefix caching, when enabled (``prefix_groups > 0``): requests of a group
+  start with the group's shared prompt prefix; every full block of that
+  prefix, once its K/V are in the cache, is registered under a key, and a
+  later request with the same prefix takes the same physical page into its
+  block table (refcounted) and starts its prefill after the shared blocks.
+  A page whose last user frees it keeps its key and content until an
+  allocation finds no uninitialized page and demotes the most recently freed
+  such page (sections "Prefix caching", "Eviction").
 
 The second policy, prefill-first (section "PrefillFirst"), finishes chunked
 prefills before it resumes decoding: active prefills first, then waiting
@@ -29,13 +37,16 @@ defaults to 0 (section "Admission").
 
 Readings (the pages leave them open): arrivals are drawn per step; a soft-reset
 request re-enters at the head of the waiting queue; prefill-first still gives
-decodes whatever token and request budget the prefills leave.
+decodes whatever token and request budget the prefills leave; a block's
+content key is (prefix group, block index), only blocks that lie wholly in the
+shared prefix are shared, and at least the prompt's last token is always
+computed.
 """
 from __future__ import annotations
 
 import dataclasses
 import math
-from collections import deque
+from collections import OrderedDict, deque
 from typing import List, Optional
 
 import numpy as np
@@ -62,6 +73,10 @@ class TraceConfig:
     dtype: str = "bf16"
     seed: int = 4
     policy: str = "fifo"        # "fifo" or "prefill_first"
+    prefix_groups: int = 0      # shared prompt prefixes (0: no prefix caching)
+    prefix_share: float = 0.75  # fraction of requests that start with a group prefix
+    prefix_len_min: int = 64
+    prefix_len_max: int = 1024
 
 
 def prefill_first_config(**kw) -> TraceConfig:
@@ -82,6 +97,10 @@ class Request:
     pages: List[int] = dataclasses.field(default_factory=list)
     finish_step: Optional[int] = None
     resets: int = 0
+    group: int = -1             # shared prompt prefix group (-1: none)
+    prefix_len: int = 0         # tokens of the group prefix at the start of the prompt
+    registered: int = 0         # prefix blocks of this request registered in the pool
+    reused_tokens: int = 0      # prompt tokens taken from cached blocks at admission
 
     @property
     def kv_len(self) -> int:
@@ -92,22 +111,64 @@ class Request:
 
 
 class PagePool:
+    """Refcounted pages. A page holding a full block of a shared prefix carries that
+    block's key; when its last user frees it, it stays as an initialized page that a
+    later request with the same prefix can take back, until an allocation finds no
+    uninitialized page and demotes the most recently freed initialized one."""
+
     def __init__(self, num_pages: int):
         self.num_pages = num_pages
-        self.free = deque(range(RESERVED_PAGES, num_pages))
+        self.free = deque(range(RESERVED_PAGES, num_pages))  # uninitialized
+        self.cached: "OrderedDict[tuple, int]" = OrderedDict()  # key -> page, refcount 0
+        self.key_of = {}   # page -> key
+        self.page_of = {}  # key -> page (in use or cached)
+        self.ref = [0] * num_pages
 
     @property
     def capacity(self) -> int:
         return self.num_pages - RESERVED_PAGES
 
     def available(self) -> int:
-        return len(self.free)
+        return len(self.free) + len(self.cached)
 
     def take(self, n: int) -> List[int]:
-        return [self.free.popleft() for _ in range(n)]
+        out = []
+        for _ in range(n):
+            if self.free:
+                p = self.free.popleft()
+            else:  # demote the most recently freed initialized page
+                key, p = self.cached.popitem(last=True)
+                del self.key_of[p]
+                del self.page_of[key]
+            self.ref[p] = 1
+            out.append(p)
+        return out
 
     def give(self, pages: List[int]):
-        self.free.extend(pages)
+        for p in pages:
+            self.ref[p] -= 1
+            if self.ref[p] == 0:
+                key = self.key_of.get(p)
+                if key is None:
+                    self.free.append(p)
+                else:
+                    self.cached[key] = p
+
+    def cached_page(self, key) -> Optional[int]:
+        return self.page_of.get(key)
+
+    def share(self, key) -> int:
+        """Take one more reference to the page that holds `key` (it must exist)."""
+        p = self.page_of[key]
+        if self.ref[p] == 0:
+            del self.cached[key]
+        self.ref[p] += 1
+        return p
+
+    def register(self, page: int, key):
+        if key not in self.page_of and page not in self.key_of:
+            self.page_of[key] = page
+            self.key_of[page] = key
 
 
 def draw_requests(cfg: TraceConfig, rng) -> List[Request]:
@@ -122,6 +183,16 @@ def draw_requests(cfg: TraceConfig, rng) -> List[Request]:
             reqs.append(Request(i, int(prompts[i]), int(outputs[i]), step))
             i += 1
         step += 1
+    if cfg.prefix_groups > 0:
+        # group prefixes from a stream of their own: the trace without them is unchanged
+        prng = np.random.default_rng(cfg.seed + 7919)
+        plens = prng.integers(cfg.prefix_len_min, cfg.prefix_len_max, endpoint=True,
+                              size=cfg.prefix_groups)
+        for req in reqs:
+            if prng.random() < cfg.prefix_share:
+                req.group = int(prng.integers(cfg.prefix_groups))
+                req.prefix_len = int(plens[req.group])
+                req.prompt_len += req.prefix_len  # the request's own text follows the prefix
     return reqs
 
 
@@ -160,6 +231,7 @@ class FifoScheduler:
             req.output_len -= req.generated
         req.generated = 0
         req.prefilled = 0
+        req.registered = 0
         req.state = "PENDING"
         self.pool.give(req.pages)
         req.pages = []
@@ -208,13 +280,20 @@ class FifoScheduler:
                 if self.pool.available() < cfg.safety_margin * self.pool.capacity:
                     break
                 req = self.waiting[0]
-                n = min(req.prompt_len, cfg.max_batch_tokens - tokens)
-                if self._pages_needed(req, n) > self.pool.available():
+                keys = self._cached_prefix(req)
+                ctx = len(keys) * cfg.block_size
+                n = min(req.prompt_len - ctx, cfg.max_batch_tokens - tokens)
+                revived = sum(1 for k in keys if self.pool.ref[self.pool.page_of[k]] == 0)
+                fresh = -(-(ctx + n) // cfg.block_size) - len(keys)
+                if fresh > self.pool.available() - revived:
                     break  # admission needs every page of the first chunk
                 self.waiting.popleft()
+                req.pages = [self.pool.share(k) for k in keys]
+                req.prefilled = ctx
+                req.reused_tokens = ctx
                 req.state = "PREFILLING"
                 self.active.append(req)
-                fit(req, 0, n)
+                fit(req, ctx, n)
 
         if cfg.policy == "prefill_first":
             active_of("PREFILLING")
@@ -226,11 +305,34 @@ class FifoScheduler:
             admit()
         return batch
 
+    def _cached_prefix(self, req: Request) -> List[tuple]:
+        """Keys of the request's leading prefix blocks already in the pool (at least the
+        prompt's last token stays to compute)."""
+        if req.group < 0:
+            return []
+        bs = self.cfg.block_size
+        keys = []
+        for k in range(min(req.prefix_len, req.prompt_len - 1) // bs):
+            if self.pool.cached_page((req.group, k)) is None:
+                break
+            keys.append((req.group, k))
+        return keys
+
+    def _register_prefix(self, req: Request):
+        """Full prefix blocks whose K/V are now in the cache become shareable."""
+        if req.group < 0:
+            return
+        full = min(req.prefilled, req.prefix_len) // self.cfg.block_size
+        for k in range(req.registered, full):
+            self.pool.register(req.pages[k], (req.group, k))
+        req.registered = max(req.registered, full)
+
     def complete(self, batch):
         """Advance every scheduled request past this step's forward pass."""
         for req, ctx, q_len in batch:
             if req.state == "PREFILLING":
                 req.prefilled += q_len
+                self._register_prefix(req)
                 if req.prefilled == req.prompt_len:
                     req.generated = 1  # the last chunk yields the first output token
                     req.state = "DECODING"
