@@ -233,7 +233,8 @@ def run_ours(args, spec, world, rank, local):
         cb.paged_attention(out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
                            md["seq_lens"], md["block_table"], spec.query_start_loc,
                            spec.seq_lens, ws, scale=spec.scale,
-                           sliding_window=spec.sliding_window, k_new=x["k_new"],
+                           sliding_window=spec.sliding_window, ring_blocks=spec.ring_blocks,
+                           k_new=x["k_new"],
                            v_new=x["v_new"], slot_mapping=md["slot_mapping"], stream=stream)
 
     for _ in range(args.warmup):
@@ -302,7 +303,8 @@ def run_ours(args, spec, world, rank, local):
         cb.paged_attention(out, dev_in["q"], x["k_cache"], x["v_cache"],
                            dev_md["query_start_loc"], dev_md["seq_lens"], dev_md["block_table"],
                            spec.query_start_loc, spec.seq_lens, ws, scale=spec.scale,
-                           sliding_window=spec.sliding_window, k_new=dev_in["k_new"],
+                           sliding_window=spec.sliding_window, ring_blocks=spec.ring_blocks,
+                           k_new=dev_in["k_new"],
                            v_new=dev_in["v_new"], slot_mapping=dev_md["slot_mapping"],
                            stream=stream)
         host_out.copy_(out, non_blocking=True)
@@ -347,7 +349,7 @@ def time_oracle(spec, budget_s: float, h=None, max_steps=None):
     while True:
         oracle.step(h["q"], h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], spec.slot_mapping,
                     spec.query_start_loc, spec.seq_lens, spec.block_table, spec.block_size,
-                    spec.scale, spec.sliding_window)
+                    spec.scale, spec.sliding_window, ring_blocks=spec.ring_blocks)
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_steps is not None and done >= max_steps):
@@ -372,7 +374,7 @@ def oracle_sample_spec(spec, max_requests=None):
 def oracle_sample_size(config):
     # requests per oracle sample so that one sample takes a few seconds at most
     return {"decode": None, "tiny_mixed": None, "mixed": 24, "long_decode": 2,
-            "long_decode_window": 8}.get(config)
+            "long_decode_window": 8, "long_decode_ring": 8}.get(config)
 
 
 # ---------------------------------------------------------------- trace (c5)

@@ -191,6 +191,38 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
                              void* stream);
 
 /*
+ * cb_paged_attention_ring -- the same step for a sliding-window layer whose pages
+ * are recycled in a ring: logical block b of request r lives in page
+ * block_table[r * block_table_stride + b % ring_blocks] (the ring of a request has
+ * ring_blocks entries; the rest of its row is unused).
+ *
+ * Sliding layers keep only a fixed window of recent tokens by reusing a small
+ * number of pages, without a full per-request block table ("Continuous batching
+ * architecture", Transformers docs, section "Memory management"). A position
+ * older than the window may have been overwritten by a newer one mapping to the
+ * same ring entry; it is never read. The caller builds slot_mapping with the same
+ * mapping (slot = page_of(p) * block_size + p % block_size).
+ *
+ * Arguments, layouts, ownership and errors as cb_paged_attention, plus:
+ * ring_blocks > 0 and <= block_table_stride, sliding_window > 0
+ * (CB_ERR_INVALID_ARG otherwise), and for every request the positions from its
+ * first query's window start max(0, context_len - sliding_window + 1) to
+ * seq_len - 1 must span at most ring_blocks blocks, so that all of them are live
+ * at once (CB_ERR_METADATA otherwise).
+ */
+cb_status cb_paged_attention_ring(void* out, const void* q, void* k_cache, void* v_cache,
+                                  const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, const int32_t* block_table,
+                                  int32_t block_table_stride, int32_t ring_blocks,
+                                  const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                                  int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                                  int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, float scale, int32_t sliding_window,
+                                  int32_t dtype, uint32_t flags, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * cb_read_error_word -- synchronise `stream`, copy the workspace error word
  * to *h_error, clear it, and return CB_ERR_DEVICE_CHECK if it was non-zero.
  */

@@ -76,9 +76,17 @@ def copy_blocks(k_dst, v_dst, k_src, v_src, src_ids, dst_ids):
         v_dst[int(d)] = v_src[int(s)]
 
 
-def resolve(block_table_row, kv_pos, block_size):
-    """Logical position -> (physical block, offset in block)."""
-    return int(block_table_row[kv_pos // block_size]), kv_pos % block_size
+def resolve(block_table_row, kv_pos, block_size, ring_blocks=0):
+    """Logical position -> (physical block, offset in block).
+
+    With ``ring_blocks > 0`` the row is a ring of recycled pages of a sliding-window
+    layer ("Continuous batching architecture", section "Memory management": sliding
+    layers keep a fixed window of recent tokens by reusing a few pages): logical
+    block b lives in entry ``b % ring_blocks``."""
+    b = kv_pos // block_size
+    if ring_blocks > 0:
+        b %= ring_blocks
+    return int(block_table_row[b]), kv_pos % block_size
 
 
 def kv_range(context_len, local_q, sliding_window):
@@ -88,12 +96,14 @@ def kv_range(context_len, local_q, sliding_window):
     return lo, hi
 
 
-def gather_request_kv(cache, block_table_row, seq_len, block_size):
-    """The request's KV in logical order, ``[seq_len, Hkv, D]`` float64, one position at a time."""
+def gather_request_kv(cache, block_table_row, seq_len, block_size, ring_blocks=0):
+    """The request's KV in logical order, ``[seq_len, Hkv, D]`` float64, one position at a time.
+    (With a ring, positions older than the ring hold whatever recycled them; the window
+    never reaches them.)"""
     _, _, hkv, d = cache.shape
     out = np.empty((seq_len, hkv, d), dtype=np.float64)
     for p in range(seq_len):
-        blk, off = resolve(block_table_row, p, block_size)
+        blk, off = resolve(block_table_row, p, block_size, ring_blocks)
         out[p] = cache[blk, off]
     return out
 
@@ -119,7 +129,7 @@ def softmax_attend(q_heads, K, V, scale):
 
 
 def paged_attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, block_size,
-                    scale, sliding_window=0, rows=None):
+                    scale, sliding_window=0, rows=None, ring_blocks=0):
     """Attention of every packed query row (or of ``rows`` only) over its request's paged KV.
 
     q: ``[T, Hq, D]``; caches ``[num_blocks, block_size, Hkv, D]`` (already
@@ -145,8 +155,8 @@ def paged_attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
             continue
         seq_len = int(seq_lens[r])
         context_len = seq_len - q_len
-        K = gather_request_kv(k_cache, block_table[r], seq_len, block_size)
-        V = gather_request_kv(v_cache, block_table[r], seq_len, block_size)
+        K = gather_request_kv(k_cache, block_table[r], seq_len, block_size, ring_blocks)
+        V = gather_request_kv(v_cache, block_table[r], seq_len, block_size, ring_blocks)
         for t in my_rows:
             local_q = t - q_start
             lo, hi = kv_range(context_len, local_q, sliding_window)
@@ -157,7 +167,7 @@ def paged_attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
 
 
 def step(q, k_cache, v_cache, k_new, v_new, slot_mapping, query_start_loc, seq_lens, block_table,
-         block_size, scale, sliding_window=0, rows=None):
+         block_size, scale, sliding_window=0, rows=None, ring_blocks=0):
     """One step: scatter the new K/V (on copies of the caches), then attend.
 
     Returns (out float64 [T, Hq, D], k_cache', v_cache').
@@ -166,5 +176,5 @@ def step(q, k_cache, v_cache, k_new, v_new, slot_mapping, query_start_loc, seq_l
     vc = np.array(v_cache, copy=True)
     scatter_kv(kc, vc, k_new, v_new, slot_mapping)
     out = paged_attention(q, kc, vc, query_start_loc, seq_lens, block_table, block_size, scale,
-                          sliding_window, rows)
+                          sliding_window, rows, ring_blocks)
     return out, kc, vc

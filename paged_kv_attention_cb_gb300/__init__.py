@@ -55,6 +55,10 @@ _SIGNATURES = {
         _i32, _i32, _i32,              # Hq, Hkv, D
         ctypes.c_float, _i32, _i32,    # scale, sliding_window, dtype
         ctypes.c_uint32, _vp, ctypes.c_size_t, _vp]),  # flags, workspace, bytes, stream
+    "cb_paged_attention_ring": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,  # ... stride, ring_blocks
+        _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+        ctypes.c_float, _i32, _i32, ctypes.c_uint32, _vp, ctypes.c_size_t, _vp]),
     "cb_read_error_word": (ctypes.c_int, [_vp, _vp, _vp]),
     "cb_paged_attention_no_alloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
@@ -165,11 +169,14 @@ def read_error_word(workspace, stream=None) -> int:
 
 def paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
                     h_query_start_loc, h_seq_lens, workspace, *, scale=0.0, sliding_window=0,
-                    k_new=None, v_new=None, slot_mapping=None, flags=0, stream=None):
+                    k_new=None, v_new=None, slot_mapping=None, flags=0, stream=None,
+                    ring_blocks=0):
     """One ragged paged-attention step (see cb_paged_attention in include/cb.h).
 
     out, q: [T, Hq, D]; caches [NB, BS, Hkv, D]; device metadata int32 (slot_mapping
     int64); h_query_start_loc / h_seq_lens: host copies of the same metadata.
+    ring_blocks > 0: a sliding-window layer whose pages are recycled in a ring
+    (cb_paged_attention_ring): logical block b at block_table[r, b % ring_blocks].
     """
     T, Hq, D = q.shape
     NB, BS, Hkv, _ = k_cache.shape
@@ -179,12 +186,16 @@ def paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_t
     if hq.shape[0] != R + 1 or hs.shape[0] != R:
         raise CbError(2, "host mirrors must have R+1 and R entries")
     stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
-    _check(lib().cb_paged_attention(
-        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
-        _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride,
-        hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
-        R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    head = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+            _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride)
+    tail = (hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
+            R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q),
+            int(flags), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    if ring_blocks:
+        _check(lib().cb_paged_attention_ring(*head, int(ring_blocks), *tail))
+    else:
+        _check(lib().cb_paged_attention(*head, *tail))
     return out
 
 

@@ -333,7 +333,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       int pg = 0;
       if (lane < n)
         pg = __ldg(p.a.block_table + (long long)r * p.a.bt_stride +
-                   (kb_start + lane) * kKB / p.a.block_size);
+                   bt_entry((kb_start + lane) * kKB / p.a.block_size, p.a.ring_blocks));
       return pg;
     };
     // walk state of the current segment

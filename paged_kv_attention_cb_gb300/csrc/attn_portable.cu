@@ -74,7 +74,7 @@ portable_attention_kernel(StepArgs a, int mode) {
   const T* vc = static_cast<const T*>(a.v_cache);
   const int32_t* bt = a.block_table + (int64_t)r * a.bt_stride;
   for (int p = min_kv_pos; p <= max_kv_pos; ++p) {
-    const int blk = __ldg(bt + p / a.block_size);
+    const int blk = __ldg(bt + bt_entry(p / a.block_size, a.ring_blocks));
     if (blk < 0 || blk >= a.num_blocks) {
       if (lane == 0) record_error(a.error_word, 0x1);
       continue;

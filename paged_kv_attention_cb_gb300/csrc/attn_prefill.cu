@@ -212,7 +212,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // they are used, so that the load of the next tile's ids does not stall
     auto tile_pages = [&](int j) -> int {
       const int lp = (kt0 + j) * kKeys / BS + lane;
-      return (lane < ppt && lp < npages_req) ? __ldg(bt + lp) : 0;
+      return (lane < ppt && lp < npages_req) ? __ldg(bt + bt_entry(lp, p.a.ring_blocks)) : 0;
     };
     // key tile j into `dst`: lane i loads box i (page i / kHalves, half i % kHalves
     // of head_dim); a page past the request, or past the pool, reads as zeros

@@ -144,16 +144,21 @@ cb_status cb_read_error_word(void* workspace, int32_t* h_error, void* stream) {
                    : CB_OK;
 }
 
-cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_cache,
-                             const void* k_new, const void* v_new, const int64_t* slot_mapping,
-                             const int32_t* query_start_loc, const int32_t* seq_lens,
-                             const int32_t* block_table, int32_t block_table_stride,
-                             const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
-                             int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
-                             int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
-                             int32_t head_dim, float scale, int32_t sliding_window, int32_t dtype,
-                             uint32_t flags, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The step for a plain block table (ring_blocks == 0) or a ring of recycled pages.
+cb_status paged_attention_impl(void* out, const void* q, void* k_cache, void* v_cache,
+                               const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                               const int32_t* query_start_loc, const int32_t* seq_lens,
+                               const int32_t* block_table, int32_t block_table_stride,
+                               int32_t ring_blocks, const int32_t* h_query_start_loc,
+                               const int32_t* h_seq_lens, int32_t num_requests, int32_t num_tokens,
+                               int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, float scale,
+                               int32_t sliding_window, int32_t dtype, uint32_t flags,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   // ---- arguments
   int elt = 0;
   cb_status st = check_dtype(dtype, &elt);
@@ -191,8 +196,23 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
   }
   if (h_query_start_loc[num_requests] != num_tokens)
     return fail(CB_ERR_METADATA, "query_start_loc[R] must equal num_tokens");
-  if (max_pages > block_table_stride)
+  if (ring_blocks > 0) {
+    // every position the step reads or writes, from the first query's window start
+    // to the last new token, must be live in the ring at once
+    if (ring_blocks > block_table_stride)
+      return fail(CB_ERR_METADATA, "block_table_stride is smaller than ring_blocks");
+    for (int r = 0; r < num_requests; ++r) {
+      const int32_t seq = h_seq_lens[r];
+      if (seq <= 0) continue;
+      const int32_t ctx = seq - (h_query_start_loc[r + 1] - h_query_start_loc[r]);
+      const int32_t lo = ctx - sliding_window + 1 > 0 ? ctx - sliding_window + 1 : 0;
+      if ((seq - 1) / block_size - lo / block_size + 1 > ring_blocks)
+        return fail(CB_ERR_METADATA,
+                    "ring_blocks too small for the window and this step's tokens of a request");
+    }
+  } else if (max_pages > block_table_stride) {
     return fail(CB_ERR_METADATA, "block_table_stride is smaller than ceil(seq_len / block_size)");
+  }
   if (num_tokens == 0) return CB_OK;
 
   if (!out || !q || !k_cache || !v_cache || !query_start_loc || !seq_lens || !block_table)
@@ -224,6 +244,7 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
   a.seq_lens = seq_lens;
   a.block_table = block_table;
   a.bt_stride = block_table_stride;
+  a.ring_blocks = ring_blocks;
   a.num_requests = num_requests;
   a.num_tokens = num_tokens;
   a.num_blocks = num_blocks;
@@ -243,6 +264,49 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
   cudaError_t e = cb::run_plan(plan, a, s);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return CB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_cache,
+                             const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                             const int32_t* query_start_loc, const int32_t* seq_lens,
+                             const int32_t* block_table, int32_t block_table_stride,
+                             const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                             int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                             int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, float scale, int32_t sliding_window, int32_t dtype,
+                             uint32_t flags, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return paged_attention_impl(out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
+                              query_start_loc, seq_lens, block_table, block_table_stride, 0,
+                              h_query_start_loc, h_seq_lens, num_requests, num_tokens, num_blocks,
+                              block_size, num_q_heads, num_kv_heads, head_dim, scale,
+                              sliding_window, dtype, flags, workspace, workspace_bytes, stream);
+}
+
+cb_status cb_paged_attention_ring(void* out, const void* q, void* k_cache, void* v_cache,
+                                  const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, const int32_t* query_start_loc,
+                                  const int32_t* seq_lens, const int32_t* block_table,
+                                  int32_t block_table_stride, int32_t ring_blocks,
+                                  const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                                  int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                                  int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, float scale, int32_t sliding_window,
+                                  int32_t dtype, uint32_t flags, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (ring_blocks <= 0) return fail(CB_ERR_INVALID_ARG, "ring_blocks must be positive");
+  if (sliding_window <= 0)
+    return fail(CB_ERR_INVALID_ARG, "a ring of recycled pages needs a sliding window");
+  return paged_attention_impl(out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
+                              query_start_loc, seq_lens, block_table, block_table_stride,
+                              ring_blocks, h_query_start_loc, h_seq_lens, num_requests,
+                              num_tokens, num_blocks, block_size, num_q_heads, num_kv_heads,
+                              head_dim, scale, sliding_window, dtype, flags, workspace,
+                              workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -28,6 +28,13 @@ template <> struct Elt<__nv_bfloat16> {
   static CB_DEV __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Block-table entry of logical block `b`: entry b of the request's row, or, for a
+// sliding layer whose pages are recycled in a ring of `ring` pages ("Continuous
+// batching architecture", Transformers docs, section "Memory management": sliding
+// layers keep only a window of recent tokens by reusing a small number of pages),
+// entry b % ring.
+CB_DEV int bt_entry(int b, int ring) { return ring > 0 ? b % ring : b; }
+
 // log2(e): the kernels keep scores in the base-2 domain (exp2 on the SFU).
 constexpr float kLog2e = 1.4426950408889634f;
 

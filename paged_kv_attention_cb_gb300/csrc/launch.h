@@ -14,6 +14,7 @@ struct StepArgs {
   const int32_t* seq_lens;
   const int32_t* block_table;
   int32_t bt_stride;
+  int32_t ring_blocks;  // 0: plain block table; > 0: logical block b at entry b % ring_blocks
   int32_t num_requests;
   int32_t num_tokens;
   int32_t num_blocks;

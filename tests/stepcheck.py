@@ -41,7 +41,8 @@ class GpuStep:
                            sliding_window=s.sliding_window,
                            k_new=self.x["k_new"] if scatter else None,
                            v_new=self.x["v_new"] if scatter else None,
-                           slot_mapping=self.md["slot_mapping"] if scatter else None, flags=flags)
+                           slot_mapping=self.md["slot_mapping"] if scatter else None, flags=flags,
+                           ring_blocks=s.ring_blocks)
         return out
 
 
@@ -51,7 +52,7 @@ def oracle_step(spec, h, rows=None, scale=None):
     return oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], spec.query_start_loc,
                                   spec.seq_lens, spec.block_table, spec.block_size,
                                   spec.scale if scale is None else scale, spec.sliding_window,
-                                  rows=rows)
+                                  rows=rows, ring_blocks=spec.ring_blocks)
 
 
 def compare(spec, got, ref, rows=None, max_abs=None, mean_abs=None):

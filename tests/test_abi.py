@@ -127,3 +127,34 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setenv("CB_LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         cb.lib()
+
+
+def call_ring(lib, qsl, seq, ring, *, window=64, BS=16, stride=None, NB=40, Hq=4, Hkv=2, D=64):
+    qsl = np.ascontiguousarray(qsl, dtype=np.int32)
+    seq = np.ascontiguousarray(seq, dtype=np.int32)
+    R, T = len(seq), int(qsl[-1])
+    stride = ring if stride is None else stride
+    return lib.cb_paged_attention_ring(
+        FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, stride, ring,
+        qsl.ctypes.data_as(ctypes.c_void_p), seq.ctypes.data_as(ctypes.c_void_p), R, T, NB, BS,
+        Hq, Hkv, D, 0.0, window, 0, 0, FAKE, lib.cb_workspace_size(R, T, Hq, Hkv, D), None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(qsl=[0, 1], seq=[1000], ring=0), 1),                  # no ring
+    (dict(qsl=[0, 1], seq=[1000], ring=5, window=0), 1),        # a ring needs a window
+    (dict(qsl=[0, 1], seq=[1000], ring=5, stride=4), 2),        # row shorter than the ring
+    (dict(qsl=[0, 1], seq=[1000], ring=4, window=64), 2),       # window 64 spans 5 blocks here
+    (dict(qsl=[0, 40], seq=[1000], ring=6, window=64), 2),      # + 40 new tokens: 7 blocks
+    (dict(qsl=[0, 0], seq=[1000], ring=4, window=64), 2),       # checked even with T = 0
+])
+def test_ring_validation_rejects(lib, kwargs, status):
+    assert call_ring(lib, **kwargs) == status
+    assert lib.cb_last_error_message()
+
+
+def test_ring_validation_accepts_exact_fit(lib):
+    # T = 0 (nothing to launch): a request at 1000 positions, window 64, reads blocks
+    # 58..62, so a ring of 5 pages fits; 40 new tokens after 960 positions span 56..62
+    assert call_ring(lib, qsl=[0, 0], seq=[1000], ring=5, window=64) == 0
+    assert call_ring(lib, qsl=[0, 0], seq=[1000], ring=7, window=104) == 0

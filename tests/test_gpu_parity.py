@@ -255,3 +255,31 @@ def test_prefill_fast_equals_portable_path():
     torch.cuda.synchronize()
     err = (fast - port).abs()
     assert float(err.max()) <= 2e-2 and float(err.mean()) <= 2e-3
+
+
+# ------------------------------------------------------------------ ring-recycled sliding pages
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("D", [64, 128])
+def test_ring_recycled_sliding_pages(path, D):
+    """Sliding-window layer on rings of recycled pages: decodes, a chunk whose queries
+    span several windows, a prompt start; the step's tokens scattered through the ring."""
+    spec = workloads.ring_step([1, 1, 200, 1, 37, 64], [3000, 129, 500, 0, 2000, 0], window=300,
+                               num_q_heads=16, num_kv_heads=4, head_dim=D, seed=D + 5)
+    assert spec.ring_blocks < spec.seq_lens.max() // spec.block_size
+    full_check(spec, flags=PATHS[path])
+
+
+@pytest.mark.parametrize("BS", [8, 16, 64])
+def test_ring_with_spare_entries(BS):
+    base = workloads.ring_step([1, 130, 1], [777, 300, 64], window=96, block_size=BS, seed=BS)
+    spec = workloads.ring_step([1, 130, 1], [777, 300, 64], window=96, block_size=BS, seed=BS,
+                               ring_blocks=base.ring_blocks + 3)
+    full_check(spec)
+
+
+def test_long_decode_ring_full_size():
+    spec = workloads.long_decode_ring()
+    assert spec.ring_blocks == 256 and spec.block_table.shape[1] == 256  # window 4096 from 28672
+    sampled_check(spec, n_rows=16)

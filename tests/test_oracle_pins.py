@@ -360,8 +360,8 @@ MUTANTS = {
     "causal bound one too far": ("kv_range", lambda c, i, w: (0 if w <= 0 else max(0, c + i - w + 1), c + i + 1)),
     "window off by one": ("kv_range", lambda c, i, w: (0 if w <= 0 else max(0, c + i - w), c + i)),
     "context dropped": ("kv_range", lambda c, i, w: (c if w <= 0 else max(c, c + i - w + 1), c + i)),
-    "block index uses offset": ("resolve", lambda row, p, bs: (int(row[p % bs]), p // bs)),
-    "offset ignores block": ("resolve", lambda row, p, bs: (int(row[0]), p % bs)),
+    "block index uses offset": ("resolve", lambda row, p, bs, ring=0: (int(row[p % bs]), p // bs)),
+    "offset ignores block": ("resolve", lambda row, p, bs, ring=0: (int(row[0]), p % bs)),
     "no scale": ("softmax_attend", lambda qh, K, V, s: _attend(qh, K, V, 1.0)),
     "scale squared": ("softmax_attend", lambda qh, K, V, s: _attend(qh, K, V, s * s)),
     "softmax over heads": ("softmax_attend", lambda qh, K, V, s: _attend_wrong_axis(qh, K, V, s)),
@@ -518,3 +518,62 @@ def test_shared_prefix_pages_equal_private_copies():
                                   spec.block_size, spec.scale)
     t1 = int(spec.query_start_loc[1])
     assert not np.array_equal(out_wrong[t1:], out_shared[t1:])
+
+
+# ------------------------------------------------------------------ ring-recycled sliding pages
+
+
+def _ring_layout(spec, x, ring, rng):
+    """The plain case's logical K/V laid out in rings of `ring` pages per request: the
+    window's positions hold their values; older positions of the ring hold garbage."""
+    bs, R = spec.block_size, spec.R
+    nb = workloads.RESERVED_PAGES + R * ring
+    shape = (nb, bs) + x["k_cache"].shape[2:]
+    kc = rng.standard_normal(shape) * 1e3  # garbage everywhere first
+    vc = rng.standard_normal(shape) * 1e3
+    pages = workloads.RESERVED_PAGES + rng.permutation(R * ring)
+    bt = pages.reshape(R, ring).astype(np.int32)
+    slots = spec.slot_mapping.copy()
+    for r in range(R):
+        ctx, seq = int(spec.ctx_lens[r]), int(spec.seq_lens[r])
+        lo = max(0, ctx - spec.sliding_window + 1)
+        for p in range((lo // bs) * bs, ctx):  # context positions the step can read
+            e = (p // bs) % ring
+            kc[bt[r, e], p % bs] = x["logical_k"][r][p]
+            vc[bt[r, e], p % bs] = x["logical_v"][r][p]
+        t0 = int(spec.query_start_loc[r])
+        for i in range(seq - ctx):  # the step's new tokens go through the ring too
+            p = ctx + i
+            slots[t0 + i] = int(bt[r, (p // bs) % ring]) * bs + p % bs
+    return kc, vc, bt, slots
+
+
+def test_ring_covering_every_block_equals_the_plain_table():
+    spec, x = make_case([3, 1, 6], [20, 37, 9], 8, 2, 8, 4, seed=61, window=11)
+    out, _, _ = run_oracle(spec, x)
+    out_r, _, _ = oracle.step(x["q"], x["k_cache"], x["v_cache"], x["k_new"], x["v_new"],
+                              spec.slot_mapping, spec.query_start_loc, spec.seq_lens,
+                              spec.block_table, spec.block_size, spec.scale, spec.sliding_window,
+                              ring_blocks=spec.block_table.shape[1])
+    assert np.array_equal(out, out_r)
+
+
+@pytest.mark.parametrize("window,extra", [(11, 0), (7, 2), (1, 0)])
+def test_ring_layout_equals_plain_layout(window, extra):
+    spec, x = make_case([3, 1, 6, 2], [20, 37, 9, 0], 8, 2, 8, 4, seed=62, window=window)
+    out, _, _ = run_oracle(spec, x)
+    bs = spec.block_size
+    need = max((int(spec.seq_lens[r]) - 1) // bs
+               - max(0, int(spec.ctx_lens[r]) - window + 1) // bs + 1 for r in range(spec.R))
+    ring = need + extra
+    kc, vc, bt, slots = _ring_layout(spec, x, ring, np.random.default_rng(3))
+    out_r, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], slots, spec.query_start_loc,
+                              spec.seq_lens, bt, bs, spec.scale, window, ring_blocks=ring)
+    assert np.array_equal(out, out_r)
+    # a ring index off by one reads the garbage and the output moves
+    if ring > 1:
+        bad = np.roll(bt, 1, axis=1)
+        out_b, _, _ = oracle.step(x["q"], kc, vc, x["k_new"], x["v_new"], slots,
+                                  spec.query_start_loc, spec.seq_lens, bad, bs, spec.scale, window,
+                                  ring_blocks=ring)
+        assert not np.allclose(out, out_b)

@@ -52,6 +52,7 @@ class StepSpec:
     sliding_window: int = 0
     seed: int = 0
     q_std: float = 1.0  # Q ~ N(0, q_std^2); K, V ~ N(0, 1)
+    ring_blocks: int = 0  # > 0: sliding layer, logical block b at block_table[r, b % ring_blocks]
 
     @property
     def R(self) -> int:
@@ -152,6 +153,55 @@ def share_prefix_pages(spec: StepSpec, donor: int, recipient: int, n_pages: int)
     bt[recipient, :n_pages] = bt[donor, :n_pages]
     return StepSpec(**{**spec.__dict__, "block_table": bt,
                        "name": f"{spec.name}_shared{donor}to{recipient}x{n_pages}"})
+
+
+def ring_step(q_lens, ctx_lens, window, *, ring_blocks=None, num_q_heads=32, num_kv_heads=8,
+              head_dim=128, block_size=16, dtype="bf16", seed=0, scale=None, pool_factor=1.2,
+              q_std=1.0, name="ring") -> StepSpec:
+    """A step of a sliding-window layer whose pages are recycled in a ring per request
+    ("Continuous batching architecture", section "Memory management": sliding layers
+    keep a fixed window of recent tokens by reusing a small number of pages).
+
+    Each request owns ``ring_blocks`` pages (default: the fewest that hold every
+    position the step reads or writes, from the first query's window start to the
+    last new token); logical block b lives in ring entry b % ring_blocks, and the
+    step's new tokens are scattered through the same mapping. Pages come from a
+    seeded permutation of the pool."""
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    ctx_lens = np.asarray(ctx_lens, dtype=np.int32)
+    R = q_lens.shape[0]
+    seq = (ctx_lens + q_lens).astype(np.int32)
+    lo = np.maximum(0, ctx_lens - window + 1)
+    span = [int((seq[r] - 1) // block_size - lo[r] // block_size + 1) for r in range(R)]
+    ring = int(ring_blocks or max(span))
+    if ring < max(span):
+        raise ValueError("ring too small for the window and the step's tokens")
+    rng = np.random.default_rng(seed)
+    num_blocks = RESERVED_PAGES + int(math.ceil(pool_factor * R * ring))
+    perm = rng.permutation(np.arange(RESERVED_PAGES, num_blocks))
+    bt = perm[:R * ring].reshape(R, ring).astype(np.int32)
+    qsl = np.zeros(R + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(q_lens)
+    slots = np.empty(int(qsl[-1]), dtype=np.int64)
+    for r in range(R):
+        for i in range(int(q_lens[r])):
+            p = int(ctx_lens[r]) + i
+            slots[qsl[r] + i] = int(bt[r, (p // block_size) % ring]) * block_size + p % block_size
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    return StepSpec(name=name, dtype=dtype, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                    head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
+                    q_lens=q_lens, ctx_lens=ctx_lens, query_start_loc=qsl, seq_lens=seq,
+                    block_table=bt, slot_mapping=slots, scale=float(scale),
+                    sliding_window=int(window), seed=seed, q_std=q_std, ring_blocks=ring)
+
+
+def long_decode_ring(seed: int = 3, window: int = 4096) -> StepSpec:
+    """long_decode_window on a sliding layer with ring-recycled pages: 16 requests at
+    seq_len 32768, window 4096 (positions 28672..32767): 256 pages of 16 tokens per request
+    instead of 2048."""
+    return ring_step(np.ones(16, np.int32), np.full(16, 32767, np.int32), window, num_q_heads=64,
+                     num_kv_heads=8, seed=seed, name=f"long_decode_16x32768_window{window}_ring")
 
 
 def tiny_mixed(seed: int = 0) -> StepSpec:
@@ -256,6 +306,7 @@ CONFIGS = {
     "mixed": mixed_step,
     "long_decode": long_decode,
     "long_decode_window": lambda seed=3: long_decode(seed, window=4096),
+    "long_decode_ring": long_decode_ring,
 }
 
 
