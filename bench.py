@@ -55,6 +55,7 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 FLUSH_BYTES = 512 << 20
+GRAPH_Q_INTERVAL = 64  # query padding interval of --graph (the decode step's 64 requests fit)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -218,6 +219,11 @@ def run_ours(args, spec, world, rank, local):
                             dev)
     out = torch.empty_like(x["q"])
     flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    graph = None
+    if args.graph:
+        # graphs need a created stream; the step's buffers are the persistent ones above
+        graph = cb.GraphCache(q_interval=GRAPH_Q_INTERVAL)
+        torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
 
     class Flush:
@@ -229,13 +235,26 @@ def run_ours(args, spec, world, rank, local):
 
     flush = Flush()
 
-    def step():
+    def attention(*a, **k):
+        if graph is None:
+            return cb.paged_attention(*a, ring_blocks=spec.ring_blocks, **k)
+        return cb.paged_attention_graphed(graph, *a, **k)
+
+    def eager_step():
         cb.paged_attention(out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
                            md["seq_lens"], md["block_table"], spec.query_start_loc,
                            spec.seq_lens, ws, scale=spec.scale,
                            sliding_window=spec.sliding_window, ring_blocks=spec.ring_blocks,
-                           k_new=x["k_new"],
-                           v_new=x["v_new"], slot_mapping=md["slot_mapping"], stream=stream)
+                           k_new=x["k_new"], v_new=x["v_new"], slot_mapping=md["slot_mapping"],
+                           stream=stream)
+
+    def step():
+        if graph is None:
+            return eager_step()
+        attention(out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
+                  md["seq_lens"], md["block_table"], spec.query_start_loc, spec.seq_lens, ws,
+                  scale=spec.scale, sliding_window=spec.sliding_window, k_new=x["k_new"],
+                  v_new=x["v_new"], slot_mapping=md["slot_mapping"], stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -277,11 +296,12 @@ def run_ours(args, spec, world, rank, local):
         torch.cuda.synchronize()
         alt_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(a0, a1)), world) / args.steps
 
-    # ---- per-kernel attribution pass (same steps, events around each launch)
+    # ---- per-kernel attribution pass (same steps, events around each launch; graph
+    # replays are not timed per kernel, so this pass runs the same kernels eagerly)
     cb.kernel_timing(True)
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        step()
+        eager_step()
     per_kernel = cb.kernel_timing_collect()
     cb.kernel_timing(False)
 
@@ -300,10 +320,10 @@ def run_ours(args, spec, world, rank, local):
             dev_in[k].copy_(host_in[k], non_blocking=True)
         for k in dev_md:
             dev_md[k].copy_(host_md[k], non_blocking=True)
-        cb.paged_attention(out, dev_in["q"], x["k_cache"], x["v_cache"],
+        attention(out, dev_in["q"], x["k_cache"], x["v_cache"],
                            dev_md["query_start_loc"], dev_md["seq_lens"], dev_md["block_table"],
                            spec.query_start_loc, spec.seq_lens, ws, scale=spec.scale,
-                           sliding_window=spec.sliding_window, ring_blocks=spec.ring_blocks,
+                           sliding_window=spec.sliding_window,
                            k_new=dev_in["k_new"],
                            v_new=dev_in["v_new"], slot_mapping=dev_md["slot_mapping"],
                            stream=stream)
@@ -323,9 +343,68 @@ def run_ours(args, spec, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(e_starts, e_stops)), world)
     barrier(world)
+    # ---- host-bound regime: steps back to back (no flush, one sync at the end)
+    def wall_us(fn, n=200):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        torch.cuda.synchronize()
+        return 1e6 * (time.perf_counter() - t0) / n
+
+    def host_us(fn, n=200):
+        fn()
+        torch.cuda.synchronize()
+        t = 0.0
+        for _ in range(n):
+            t0 = time.perf_counter()
+            fn()
+            t += time.perf_counter() - t0
+        torch.cuda.synchronize()
+        return 1e6 * t / n
+
+    graph_info = None
+    if graph is not None:
+        hq = np.ascontiguousarray(spec.query_start_loc, dtype=np.int32)
+        hs = np.ascontiguousarray(spec.seq_lens, dtype=np.int32)
+        prepared = cb.PreparedGraphStep(
+            graph, out, x["q"], x["k_cache"], x["v_cache"], md["query_start_loc"],
+            md["seq_lens"], md["block_table"], hq, hs, ws, scale=spec.scale,
+            sliding_window=spec.sliding_window, k_new=x["k_new"], v_new=x["v_new"],
+            slot_mapping=md["slot_mapping"], stream=stream)
+        graph_info = {"q_interval": GRAPH_Q_INTERVAL,
+                      "wall_us_per_step_graphed": wall_us(prepared),
+                      "wall_us_per_step_eager": wall_us(eager_step),
+                      "host_us_per_call_graphed_prepared": host_us(prepared),
+                      "host_us_per_call_graphed": host_us(step),
+                      "host_us_per_call_eager": host_us(eager_step)}
+        graph_info.update(graph.stats())
+        # a host-bound batch: 64 decodes over 16..128 positions (a few us on the device)
+        small = workloads.decode_step(seed=11, lo=16, hi=128)
+        xs = workloads.draw_tensors(small, dev)
+        mds = workloads.metadata_tensors(small, dev)
+        wss = cb.alloc_workspace(small.R, small.T, small.num_q_heads, small.num_kv_heads,
+                                 small.head_dim, dev)
+        outs = torch.empty_like(xs["q"])
+        kw = dict(scale=small.scale, k_new=xs["k_new"], v_new=xs["v_new"],
+                  slot_mapping=mds["slot_mapping"], stream=stream)
+        args_s = (outs, xs["q"], xs["k_cache"], xs["v_cache"], mds["query_start_loc"],
+                  mds["seq_lens"], mds["block_table"], small.query_start_loc, small.seq_lens, wss)
+        g2 = cb.GraphCache(q_interval=GRAPH_Q_INTERVAL)
+        prep_s = cb.PreparedGraphStep(
+            g2, outs, xs["q"], xs["k_cache"], xs["v_cache"], mds["query_start_loc"],
+            mds["seq_lens"], mds["block_table"],
+            np.ascontiguousarray(small.query_start_loc, dtype=np.int32),
+            np.ascontiguousarray(small.seq_lens, dtype=np.int32), wss, **kw)
+        graph_info["small_decode"] = {
+            "workload": small.name,
+            "wall_us_per_step_graphed": wall_us(prep_s),
+            "wall_us_per_step_eager": wall_us(lambda: cb.paged_attention(*args_s, **kw))}
+        g2.close()
     return dict(ms_per_step=ms_per_step, step_ms=step_ms, launches=launches, alt_ms=alt_ms,
                 per_kernel=per_kernel, e2e_ms_per_step=e2e_ms / args.steps, h2d=h2d, d2h=d2h,
-                clocks=clocks.summary())
+                clocks=clocks.summary(), graph=graph_info)
 
 
 # ---------------------------------------------------------------- oracle
@@ -755,6 +834,8 @@ def main():
     ap.add_argument("--config", default="decode",
                     choices=sorted(workloads.CONFIGS) + ["trace", "trace_prefill_first",
                                                          "copy_blocks"])
+    ap.add_argument("--graph", action="store_true",
+                    help="run the step through CUDA graphs cached per padded shape (decode)")
     ap.add_argument("--trace-steps", type=int, default=0,
                     help="--config trace: time only the first N steps of the trace (0: all)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -775,6 +856,10 @@ def main():
         copy_main(args, world, rank, local)
         return
     spec = workloads.by_name(args.config)
+    if args.graph and (spec.T % GRAPH_Q_INTERVAL or spec.R % GRAPH_Q_INTERVAL
+                       or spec.dtype != "bf16"):
+        raise SystemExit("--graph: the workload's R and T must be multiples of "
+                         f"{GRAPH_Q_INTERVAL} (bf16)")
     kvb = kv_bytes(spec)
     cfg = {"workload": spec.name, "requests": spec.R, "query_tokens": spec.T,
            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
@@ -784,6 +869,8 @@ def main():
            "l2": ("inputs larger than L2; 512 MiB read between timed steps (L2 evicted, clean)"
                   if args.flush == "read" else "flushed (512 MiB write) between timed steps"),
            "parallelism": f"replicas x{world}"}
+    if args.graph:
+        cfg["cuda_graphs"] = f"cached per padded shape, q_interval {GRAPH_Q_INTERVAL}"
 
     if args.impl == "reference":
         if rank != 0:
@@ -861,6 +948,8 @@ def main():
             "gpu_launches": res["launches"],
             "per_kernel_ms": {k: v[0] / v[1] for k, v in pk.items()},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": res["clocks"]}
+    if res.get("graph"):
+        line["graph"] = res["graph"]
     print(json.dumps(line), flush=True)
 
 

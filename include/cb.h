@@ -223,6 +223,62 @@ cb_status cb_paged_attention_ring(void* out, const void* q, void* k_cache, void*
                                   size_t workspace_bytes, void* stream);
 
 /*
+ * CUDA graphs of the step, one per padded shape.
+ *
+ * Every step costs CPU time to assemble and launch; recording the GPU work once
+ * and replaying it for batches of the same padded shape removes that cost. The
+ * query length is padded to a multiple of q_padding_interval_size and the KV
+ * length to a multiple of kv_padding_interval_size; recorded graphs are kept in a
+ * cache and a batch whose padded shape matches one is replayed without CPU
+ * scheduling, while a new shape triggers a capture ("Continuous batching
+ * architecture", Transformers docs, section "CUDA graphs").
+ *
+ * cb_graph_cache_create -- an empty cache; q_interval > 0 (the query-length
+ * padding interval), kv_interval >= 0 (the KV-length bucket; 0: one bucket, as
+ * the launches here do not depend on the KV length). Owned by the caller, freed
+ * with cb_graph_cache_destroy (which destroys its graphs). Not tied to a device
+ * until the first call; all calls on one cache must use the same device.
+ */
+typedef struct cb_graph_cache cb_graph_cache;
+cb_status cb_graph_cache_create(int32_t q_interval, int32_t kv_interval, cb_graph_cache** cache);
+void cb_graph_cache_destroy(cb_graph_cache* cache);
+/* Number of graphs held, captures made and replays served; any pointer may be NULL. */
+cb_status cb_graph_cache_stats(cb_graph_cache* cache, int64_t* graphs, int64_t* captures,
+                               int64_t* replays);
+
+/*
+ * cb_paged_attention_graphed -- cb_paged_attention, captured into a CUDA graph the
+ * first time its key is seen and replayed afterwards. The key is every buffer
+ * pointer, every size, num_requests and num_tokens (the padded counts), the
+ * KV-length bucket and whether the batch has decode rows and prefill rows (so a
+ * graph holds only the launches its batches need); the metadata values are read on the device at
+ * replay (the decode kernel sums its work and the prefill kernel finds its tiles
+ * there), so one graph serves every batch of its shape. Arguments as
+ * cb_paged_attention, with the padded shape:
+ *   num_requests and num_tokens multiples of q_interval (CB_ERR_INVALID_ARG);
+ *   requests past the real ones have q_len 0 and seq_len 0; tokens past
+ *   query_start_loc[R] are padding (slot_mapping -1, their out rows untouched);
+ *   query_start_loc[R] <= num_tokens.
+ * The caller keeps the buffers alive and in place while the cache holds graphs
+ * that name them, writes each step's inputs into them before the call, and must
+ * not pass the legacy default stream. Supported: bf16 with shapes that the split-KV
+ * decode and the tile prefill kernels both cover (CB_ERR_UNSUPPORTED otherwise).
+ * Per-kernel timing (cb_kernel_timing) does not see replayed kernels; the launch
+ * counts do. Thread-safe per cache (one mutex).
+ */
+cb_status cb_paged_attention_graphed(cb_graph_cache* cache, void* out, const void* q,
+                                     void* k_cache, void* v_cache, const void* k_new,
+                                     const void* v_new, const int64_t* slot_mapping,
+                                     const int32_t* query_start_loc, const int32_t* seq_lens,
+                                     const int32_t* block_table, int32_t block_table_stride,
+                                     const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                                     int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, float scale, int32_t sliding_window,
+                                     int32_t dtype, uint32_t flags, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * cb_read_error_word -- synchronise `stream`, copy the workspace error word
  * to *h_error, clear it, and return CB_ERR_DEVICE_CHECK if it was non-zero.
  */

@@ -59,6 +59,15 @@ _SIGNATURES = {
         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,  # ... stride, ring_blocks
         _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
         ctypes.c_float, _i32, _i32, ctypes.c_uint32, _vp, ctypes.c_size_t, _vp]),
+    "cb_graph_cache_create": (ctypes.c_int, [_i32, _i32, ctypes.POINTER(ctypes.c_void_p)]),
+    "cb_graph_cache_destroy": (None, [_vp]),
+    "cb_graph_cache_stats": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int64),
+                                            ctypes.POINTER(ctypes.c_int64),
+                                            ctypes.POINTER(ctypes.c_int64)]),
+    "cb_paged_attention_graphed": (ctypes.c_int, [_vp] + [
+        _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+        _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _i32, ctypes.c_uint32,
+        _vp, ctypes.c_size_t, _vp]),
     "cb_read_error_word": (ctypes.c_int, [_vp, _vp, _vp]),
     "cb_paged_attention_no_alloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
@@ -197,6 +206,97 @@ def paged_attention(out, q, k_cache, v_cache, query_start_loc, seq_lens, block_t
     else:
         _check(lib().cb_paged_attention(*head, *tail))
     return out
+
+
+class GraphCache:
+    """CUDA graphs of the step, one per padded shape (cb_graph_cache in include/cb.h)."""
+
+    def __init__(self, q_interval=64, kv_interval=0):
+        h = ctypes.c_void_p()
+        _check(lib().cb_graph_cache_create(int(q_interval), int(kv_interval), ctypes.byref(h)))
+        self._h = h
+        self.q_interval = int(q_interval)
+
+    def close(self):
+        if self._h:
+            lib().cb_graph_cache_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def stats(self):
+        g, c, r = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().cb_graph_cache_stats(self._h, ctypes.byref(g), ctypes.byref(c),
+                                          ctypes.byref(r)))
+        return {"graphs": g.value, "captures": c.value, "replays": r.value}
+
+
+def paged_attention_graphed(cache, out, q, k_cache, v_cache, query_start_loc, seq_lens,
+                            block_table, h_query_start_loc, h_seq_lens, workspace, *, scale=0.0,
+                            sliding_window=0, k_new=None, v_new=None, slot_mapping=None, flags=0,
+                            stream=None):
+    """paged_attention through a GraphCache: the buffers hold the padded shape (R and T
+    multiples of the cache's q_interval; padding requests q_len 0 / seq_len 0, padding
+    tokens past query_start_loc[R] with slot -1)."""
+    T, Hq, D = q.shape
+    NB, BS, Hkv, _ = k_cache.shape
+    R = int(seq_lens.shape[0])
+    hq = _host_i32(h_query_start_loc)
+    hs = _host_i32(h_seq_lens)
+    if hq.shape[0] != R + 1 or hs.shape[0] != R:
+        raise CbError(2, "host mirrors must have R+1 and R entries")
+    stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+    _check(lib().cb_paged_attention_graphed(
+        cache._h, _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+        _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride,
+        hq.ctypes.data_as(ctypes.c_void_p), hs.ctypes.data_as(ctypes.c_void_p),
+        R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+class PreparedGraphStep:
+    """paged_attention_graphed with the argument marshalling done once.
+
+    For a serving loop over persistent buffers: the caller writes each step's inputs
+    into the same device tensors and the same host-mirror arrays (numpy int32,
+    updated in place), then calls the object; each call is one C call (a replay, or a
+    capture for a new padded shape). The padded counts R and T are fixed by the
+    tensors' shapes.
+    """
+
+    def __init__(self, cache, out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                 h_query_start_loc, h_seq_lens, workspace, *, scale=0.0, sliding_window=0,
+                 k_new=None, v_new=None, slot_mapping=None, flags=0, stream=None):
+        import numpy as np
+
+        T, Hq, D = q.shape
+        NB, BS, Hkv, _ = k_cache.shape
+        R = int(seq_lens.shape[0])
+        for h, n in ((h_query_start_loc, R + 1), (h_seq_lens, R)):
+            if not (isinstance(h, np.ndarray) and h.dtype == np.int32 and h.flags.c_contiguous
+                    and h.shape == (n,)):
+                raise ValueError("host mirrors must be contiguous int32 numpy arrays of R+1 / R")
+        self._keep = (cache, out, q, k_cache, v_cache, query_start_loc, seq_lens, block_table,
+                      h_query_start_loc, h_seq_lens, workspace, k_new, v_new, slot_mapping)
+        stride = int(block_table.shape[1]) if block_table.dim() == 2 else 0
+        self._fn = lib().cb_paged_attention_graphed
+        self._args = (
+            cache._h, _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+            _ptr(slot_mapping), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), stride,
+            h_query_start_loc.ctypes.data_as(ctypes.c_void_p),
+            h_seq_lens.ctypes.data_as(ctypes.c_void_p), R, T, NB, BS, Hq, Hkv, D, float(scale),
+            int(sliding_window), _dtype_code(q), int(flags), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != 0:
+            _check(status)
 
 
 NO_ALLOC_SCRATCH_BYTES = 8 << 20

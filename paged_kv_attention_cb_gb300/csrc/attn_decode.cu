@@ -74,6 +74,7 @@ struct DecodeSmem {
   SegDesc seg[2];
   SegDesc done[kDoneRing];
   long long scan[16];
+  long long total_u;
   int pend[kDoneRing];
   int npend;
   int first_r;
@@ -224,8 +225,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int nthreads = blockDim.x;
   const int b = blockIdx.x;
   const int hg = blockIdx.y;
-  const int C = p.num_ctas;
-  const long long U = p.total_units;
+  int C = p.num_ctas;
+  long long U = p.total_units;
   const int R = p.a.num_requests;
 
   if (threadIdx.x == 0) {
@@ -256,6 +257,29 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // is the step's first kernel and every thread waits.
   if (!p.metadata_ready) grid_dependency_wait();
   __syncthreads();
+  if (p.units_on_device) {
+    // the decode requests' key blocks, summed over the step from the device metadata
+    long long part = 0;
+    for (int r = threadIdx.x; r < R; r += nthreads) {
+      int seq = 0, t = 0;
+      part += decode_units(p, r, &seq, &t);
+    }
+    part = warp_incl_scan(part);
+    if (lane == 31) sm.scan[warp] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long tot = 0;
+      for (int w = 0; w < (nthreads >> 5); ++w) tot += sm.scan[w];
+      sm.total_u = tot;
+    }
+    __syncthreads();
+    U = sm.total_u;
+    __syncthreads();  // sm.scan is reused by the start search below
+    // the launch has a CTA per SM; a step with fewer key blocks uses the first U of
+    // them (every CTA of the partition keeps at least one block), the rest have none
+    if (U < C) C = (int)U;
+    if (b >= C) return;  // uniform over the CTA; no pipeline started
+  }
 
   const long long u_lo = (long long)b * U / C;
   const long long u_hi = (long long)(b + 1) * U / C;
@@ -763,6 +787,29 @@ cudaError_t launch_d(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorM
 size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes) {
   return 1024 /* alignment slack */ + (size_t)stages * stage_bytes + 2 * (size_t)q_slot_bytes +
          sizeof(DecodeSmem);
+}
+
+cudaError_t prepare_decode(const DecodeArgs& p) {
+  const int G = p.a.num_q_heads / p.a.num_kv_heads;
+  auto set = [](auto kern) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemLimit);
+  };
+  if (p.a.head_dim == 64) {
+    switch (G) {
+      case 1: return set(decode_split_kernel<64, 1>);
+      case 2: return set(decode_split_kernel<64, 2>);
+      case 4: return set(decode_split_kernel<64, 4>);
+      case 8: return set(decode_split_kernel<64, 8>);
+    }
+  } else {
+    switch (G) {
+      case 1: return set(decode_split_kernel<128, 1>);
+      case 2: return set(decode_split_kernel<128, 2>);
+      case 4: return set(decode_split_kernel<128, 4>);
+      case 8: return set(decode_split_kernel<128, 8>);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(DecodeArgs p, const DecodePlan& plan, cudaStream_t stream) {

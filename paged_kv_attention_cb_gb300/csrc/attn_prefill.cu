@@ -141,11 +141,59 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Work w = work_of(p, blockIdx.x);
-  if (w.e < 0) return;  // uniform over the CTA, before any barrier
+  Work w;
+  PrefillEntry ent;
+  if (p.device_work) {
+    // request order; every request with q_len > 1 gets ceil(n_qtiles / 2) * Hkv CTAs
+    grid_dependency_wait();
+    __shared__ int s_tot[kThreads / 32];
+    __shared__ int s_hit[2];
+    const int Hkv = p.a.num_kv_heads;
+    if (threadIdx.x == 0) s_hit[0] = -1;
+    int carry = 0;
+    for (int base_r = 0; base_r < p.a.num_requests; base_r += kThreads) {
+      const int rr = base_r + threadIdx.x;
+      int n = 0;
+      if (rr < p.a.num_requests) {
+        const int ql = __ldg(p.a.query_start_loc + rr + 1) - __ldg(p.a.query_start_loc + rr);
+        if (ql > 1) n = ((ql + p.tile_tokens - 1) / p.tile_tokens + 1) / 2 * Hkv;
+      }
+      int v = n;  // inclusive warp scan
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (lane == 31) s_tot[warp] = v;
+      __syncthreads();
+      int before = carry;
+      for (int k = 0; k < warp; ++k) before += s_tot[k];
+      const int incl = before + v;
+      if (n > 0 && incl - n <= (int)blockIdx.x && (int)blockIdx.x < incl) {
+        s_hit[0] = rr;
+        s_hit[1] = (int)blockIdx.x - (incl - n);
+      }
+      for (int k = 0; k < kThreads / 32; ++k) carry += s_tot[k];
+      __syncthreads();
+      if (s_hit[0] >= 0) break;
+    }
+    if (s_hit[0] < 0) return;  // past the step's work: uniform over the CTA
+    const int rr = s_hit[0];
+    const int k = s_hit[1];
+    ent.r = rr;
+    ent.q_start = __ldg(p.a.query_start_loc + rr);
+    ent.q_len = __ldg(p.a.query_start_loc + rr + 1) - ent.q_start;
+    ent.seq_len = __ldg(p.a.seq_lens + rr);
+    ent.n_qtiles = (ent.q_len + p.tile_tokens - 1) / p.tile_tokens;
+    const int npairs = (ent.n_qtiles + 1) / 2;
+    w = Work{0, k % Hkv, npairs - 1 - k / Hkv};
+  } else {
+    w = work_of(p, blockIdx.x);
+    if (w.e < 0) return;  // uniform over the CTA, before any barrier
+    ent = p.entries[w.e];
+  }
 
   // ---- request geometry
-  const PrefillEntry& ent = p.entries[w.e];
   const int r = ent.r;
   const int g = w.g;
   const int q_start = ent.q_start;
@@ -564,6 +612,22 @@ size_t prefill_smem_bytes(int head_dim) {
 
 int prefill_ctas(int n_qtiles, int num_kv_heads) {
   return ((n_qtiles + kTiles - 1) / kTiles) * num_kv_heads;
+}
+
+int prefill_ctas_bound(int num_tokens, int num_requests, int tile_tokens, int num_kv_heads) {
+  // over the n <= min(R, T / 2) requests with q_len > 1:
+  // sum of ceil(ceil(q_len / TQ) / 2) <= (sum q_len / TQ + 2 n) / 2
+  const long long n = num_requests < num_tokens / 2 ? num_requests : num_tokens / 2;
+  const long long tiles = (long long)num_tokens / tile_tokens + 2 * n;
+  return (int)((tiles + 1) / 2) * num_kv_heads;
+}
+
+cudaError_t prepare_prefill(int head_dim) {
+  if (head_dim == 64)
+    return cudaFuncSetAttribute(prefill_tile_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<64>());
+  return cudaFuncSetAttribute(prefill_tile_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<128>());
 }
 
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream) {

@@ -5,7 +5,11 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <cstring>
+#include <mutex>
+#include <new>
 #include <string>
+#include <unordered_map>
 
 #include "cb.h"
 #include "launch.h"
@@ -35,6 +39,30 @@ cb_status check_dtype(int32_t dtype, int* elt) {
   if (dtype == CB_F32) { *elt = 4; return CB_OK; }
   if (dtype == CB_BF16) { *elt = 2; return CB_OK; }
   return fail(CB_ERR_INVALID_ARG, "dtype must be CB_F32 or CB_BF16");
+}
+
+}  // namespace
+
+// Captured steps of one padded shape each: cudaGraphExec_t by key (every buffer
+// pointer, every size, the padded counts and the KV-length bucket).
+struct cb_graph_cache {
+  int32_t q_interval = 1;
+  int32_t kv_interval = 0;
+  std::mutex mu;
+  struct Entry {
+    cudaGraphExec_t exec;
+    long long launches[cb::kNumKernels];
+  };
+  std::unordered_map<std::string, Entry> graphs;
+  long long captures = 0;
+  long long replays = 0;
+};
+
+namespace {
+
+template <typename T>
+void put(std::string& k, const T& v) {
+  k.append(reinterpret_cast<const char*>(&v), sizeof(v));
 }
 
 }  // namespace
@@ -148,8 +176,10 @@ cb_status cb_read_error_word(void* workspace, int32_t* h_error, void* stream) {
 
 namespace {
 
-// The step for a plain block table (ring_blocks == 0) or a ring of recycled pages.
-cb_status paged_attention_impl(void* out, const void* q, void* k_cache, void* v_cache,
+// The step for a plain block table (ring_blocks == 0) or a ring of recycled pages;
+// with `graph`, captured once per padded shape and replayed.
+cb_status paged_attention_impl(cb_graph_cache* graph, void* out, const void* q, void* k_cache,
+                               void* v_cache,
                                const void* k_new, const void* v_new, const int64_t* slot_mapping,
                                const int32_t* query_start_loc, const int32_t* seq_lens,
                                const int32_t* block_table, int32_t block_table_stride,
@@ -194,8 +224,19 @@ cb_status paged_attention_impl(void* out, const void* q, void* k_cache, void* v_
     const int64_t pages = ((int64_t)h_seq_lens[r] + block_size - 1) / block_size;
     if (pages > max_pages) max_pages = pages;
   }
-  if (h_query_start_loc[num_requests] != num_tokens)
+  if (graph) {
+    // padded shape: num_requests and num_tokens multiples of the query interval;
+    // the tokens past query_start_loc[R] (and requests with q_len 0) are padding
+    if (num_tokens % graph->q_interval != 0 || num_requests % graph->q_interval != 0)
+      return fail(CB_ERR_INVALID_ARG,
+                  "graph mode: num_requests and num_tokens must be multiples of q_interval");
+    if (h_query_start_loc[num_requests] > num_tokens)
+      return fail(CB_ERR_METADATA, "query_start_loc[R] must be <= num_tokens");
+    if (stream == nullptr)
+      return fail(CB_ERR_INVALID_ARG, "graph mode needs a created stream (not the legacy default)");
+  } else if (h_query_start_loc[num_requests] != num_tokens) {
     return fail(CB_ERR_METADATA, "query_start_loc[R] must equal num_tokens");
+  }
   if (ring_blocks > 0) {
     // every position the step reads or writes, from the first query's window start
     // to the last new token, must be live in the ring at once
@@ -224,17 +265,15 @@ cb_status paged_attention_impl(void* out, const void* q, void* k_cache, void* v_
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* error_word = static_cast<int32_t*>(workspace);
-
-  // ---- 1. scatter the step's new K/V (the attention reads them back)
-  if (k_new) {
+  // 1. scatter the step's new K/V (the attention reads them back)
+  auto scatter = [&]() -> cudaError_t {
+    if (!k_new) return cudaSuccess;
     const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * elt;
-    cudaError_t e = cb::launch_write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
-                                        (int64_t)num_blocks * block_size, (int32_t)row_bytes,
-                                        error_word, s);
-    if (e != cudaSuccess) return cuda_fail(e, "write_kv launch");
-  }
+    return cb::launch_write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
+                               (int64_t)num_blocks * block_size, (int32_t)row_bytes, error_word, s);
+  };
 
-  // ---- 2. attention
+  // 2. attention
   cb::StepArgs a;
   a.out = out;
   a.q = q;
@@ -259,10 +298,87 @@ cb_status paged_attention_impl(void* out, const void* q, void* k_cache, void* v_
   a.error_word = error_word;
 
   cb::Plan plan;
-  cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, workspace,
-                workspace_bytes);
-  cudaError_t e = cb::run_plan(plan, a, s);
-  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (!graph) {
+    cudaError_t e = scatter();
+    if (e != cudaSuccess) return cuda_fail(e, "write_kv launch");
+    cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, workspace,
+                  workspace_bytes);
+    e = cb::run_plan(plan, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    return CB_OK;
+  }
+
+  // ---- graph mode: every launch depends on the padded shape only
+  // which kinds of rows the batch has: part of the key, so that a graph holds only
+  // the launches its batches need
+  bool has_decode = false, has_prefill = false;
+  for (int r = 0; r < num_requests; ++r) {
+    const int32_t ql = h_query_start_loc[r + 1] - h_query_start_loc[r];
+    has_decode |= ql == 1 && h_seq_lens[r] > 0;
+    has_prefill |= ql > 1;
+  }
+  if ((flags & CB_FLAG_PORTABLE_ONLY) ||
+      !cb::plan_graph_step(plan, a, has_decode, has_prefill, workspace, workspace_bytes))
+    return fail(CB_ERR_UNSUPPORTED,
+                "graph mode covers bf16 steps that the split-KV decode and the tile prefill "
+                "kernels both support");
+  std::string key;
+  for (const void* ptr : {(const void*)out, q, (const void*)k_cache, (const void*)v_cache, k_new,
+                          v_new, (const void*)slot_mapping, (const void*)query_start_loc,
+                          (const void*)seq_lens, (const void*)block_table, (const void*)workspace})
+    put(key, ptr);
+  for (int32_t v : {block_table_stride, num_requests, num_tokens, num_blocks, block_size,
+                    num_q_heads, num_kv_heads, head_dim, a.sliding_window, dtype, (int32_t)flags})
+    put(key, v);
+  put(key, a.scale_log2);
+  put(key, workspace_bytes);
+  int64_t kv_bucket = 0;  // the longest sequence, padded to the KV interval
+  if (graph->kv_interval > 0) {
+    int32_t max_seq = 0;
+    for (int r = 0; r < num_requests; ++r) max_seq = h_seq_lens[r] > max_seq ? h_seq_lens[r] : max_seq;
+    kv_bucket = ((int64_t)max_seq + graph->kv_interval - 1) / graph->kv_interval;
+  }
+  put(key, kv_bucket);
+  put(key, (int32_t)(has_decode ? 1 : 0) | (has_prefill ? 2 : 0));
+
+  std::lock_guard<std::mutex> lock(graph->mu);
+  auto it = graph->graphs.find(key);
+  if (it == graph->graphs.end()) {
+    cudaError_t e = cb::prepare_plan(plan, a);
+    if (e != cudaSuccess) return cuda_fail(e, "graph kernel attributes");
+    long long before[cb::kNumKernels], after[cb::kNumKernels];
+    cb::launch_counts(before);
+    const bool timing = cb::set_kernel_timing(false);  // no event nodes in the graph
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      e = scatter();
+      if (e == cudaSuccess) e = cb::run_plan(plan, a, s);
+      const cudaError_t e2 = cudaStreamEndCapture(s, &g);
+      if (e == cudaSuccess) e = e2;
+      if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, g, 0);
+      if (g) cudaGraphDestroy(g);
+    }
+    cb::set_kernel_timing(timing);
+    cb::launch_counts(after);
+    if (e != cudaSuccess) return cuda_fail(e, "graph capture");
+    cb_graph_cache::Entry en;
+    en.exec = exec;
+    long long undo[cb::kNumKernels];
+    for (int k = 0; k < cb::kNumKernels; ++k) {
+      en.launches[k] = after[k] - before[k];
+      undo[k] = -en.launches[k];  // captured, not run: counted when the graph runs
+    }
+    cb::note_replayed_launches(undo);
+    it = graph->graphs.emplace(key, en).first;
+    ++graph->captures;
+  } else {
+    ++graph->replays;
+  }
+  cudaError_t e = cudaGraphLaunch(it->second.exec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  cb::note_replayed_launches(it->second.launches);
   return CB_OK;
 }
 
@@ -280,7 +396,7 @@ cb_status cb_paged_attention(void* out, const void* q, void* k_cache, void* v_ca
                              int32_t head_dim, float scale, int32_t sliding_window, int32_t dtype,
                              uint32_t flags, void* workspace, size_t workspace_bytes,
                              void* stream) {
-  return paged_attention_impl(out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
+  return paged_attention_impl(nullptr, out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
                               query_start_loc, seq_lens, block_table, block_table_stride, 0,
                               h_query_start_loc, h_seq_lens, num_requests, num_tokens, num_blocks,
                               block_size, num_q_heads, num_kv_heads, head_dim, scale,
@@ -301,12 +417,60 @@ cb_status cb_paged_attention_ring(void* out, const void* q, void* k_cache, void*
   if (ring_blocks <= 0) return fail(CB_ERR_INVALID_ARG, "ring_blocks must be positive");
   if (sliding_window <= 0)
     return fail(CB_ERR_INVALID_ARG, "a ring of recycled pages needs a sliding window");
-  return paged_attention_impl(out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
+  return paged_attention_impl(nullptr, out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
                               query_start_loc, seq_lens, block_table, block_table_stride,
                               ring_blocks, h_query_start_loc, h_seq_lens, num_requests,
                               num_tokens, num_blocks, block_size, num_q_heads, num_kv_heads,
                               head_dim, scale, sliding_window, dtype, flags, workspace,
                               workspace_bytes, stream);
+}
+
+cb_status cb_graph_cache_create(int32_t q_interval, int32_t kv_interval, cb_graph_cache** cache) {
+  if (!cache) return fail(CB_ERR_INVALID_ARG, "null pointer");
+  *cache = nullptr;
+  if (q_interval <= 0 || kv_interval < 0)
+    return fail(CB_ERR_INVALID_ARG, "q_interval must be positive and kv_interval >= 0");
+  cb_graph_cache* c = new (std::nothrow) cb_graph_cache();
+  if (!c) return fail(CB_ERR_INVALID_ARG, "out of host memory");
+  c->q_interval = q_interval;
+  c->kv_interval = kv_interval;
+  *cache = c;
+  return CB_OK;
+}
+
+void cb_graph_cache_destroy(cb_graph_cache* cache) {
+  if (!cache) return;
+  for (auto& kv : cache->graphs) cudaGraphExecDestroy(kv.second.exec);
+  delete cache;
+}
+
+cb_status cb_graph_cache_stats(cb_graph_cache* cache, int64_t* graphs, int64_t* captures,
+                               int64_t* replays) {
+  if (!cache) return fail(CB_ERR_INVALID_ARG, "null pointer");
+  std::lock_guard<std::mutex> lock(cache->mu);
+  if (graphs) *graphs = (int64_t)cache->graphs.size();
+  if (captures) *captures = cache->captures;
+  if (replays) *replays = cache->replays;
+  return CB_OK;
+}
+
+cb_status cb_paged_attention_graphed(cb_graph_cache* cache, void* out, const void* q,
+                                     void* k_cache, void* v_cache, const void* k_new,
+                                     const void* v_new, const int64_t* slot_mapping,
+                                     const int32_t* query_start_loc, const int32_t* seq_lens,
+                                     const int32_t* block_table, int32_t block_table_stride,
+                                     const int32_t* h_query_start_loc, const int32_t* h_seq_lens,
+                                     int32_t num_requests, int32_t num_tokens, int32_t num_blocks,
+                                     int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, float scale, int32_t sliding_window,
+                                     int32_t dtype, uint32_t flags, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (!cache) return fail(CB_ERR_INVALID_ARG, "null graph cache");
+  return paged_attention_impl(cache, out, q, k_cache, v_cache, k_new, v_new, slot_mapping,
+                              query_start_loc, seq_lens, block_table, block_table_stride, 0,
+                              h_query_start_loc, h_seq_lens, num_requests, num_tokens, num_blocks,
+                              block_size, num_q_heads, num_kv_heads, head_dim, scale,
+                              sliding_window, dtype, flags, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

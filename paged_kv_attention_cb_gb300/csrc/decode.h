@@ -23,6 +23,8 @@ struct DecodeArgs {
   int stage_bytes;        // K + V of one 16-key block for HB heads
   int q_slot_bytes;       // HB * G * D * 2
   int metadata_ready;     // the step's previous kernel is libcb's scatter
+  int units_on_device;    // total_units is summed by the kernel from the device metadata
+                          // (graph replays: nothing in the arguments depends on the batch)
   float* part_o;          // [slots][Hq][D] unnormalised partial outputs
   float2* part_ml;        // [slots][Hq] (running max in log2 units, sum)
   int* counters;          // [R][head groups] arrivals of split requests (zero between steps)
@@ -36,5 +38,7 @@ struct DecodePlan {
 
 size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes);
 cudaError_t launch_decode(DecodeArgs p, const DecodePlan& plan, cudaStream_t stream);
+// Kernel attributes the launch needs, set without launching (before a stream capture).
+cudaError_t prepare_decode(const DecodeArgs& p);
 
 }  // namespace cb

@@ -39,6 +39,11 @@ enum KernelId {
 
 void note_launch_begin(KernelId id, cudaStream_t stream);
 void note_launch_end(KernelId id, cudaStream_t stream);
+// Launch accounting for CUDA-graph replays (a replay launches what the capture recorded).
+void note_replayed_launches(const long long* per_kernel);
+void launch_counts(long long* per_kernel);
+// Per-kernel event timing of the calling thread on/off; returns the previous state.
+bool set_kernel_timing(bool enable);
 
 // Launch with the programmatic-stream-serialization attribute (the kernel may
 // start while the previous one on the stream drains; it waits on the device).

@@ -97,6 +97,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
     d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
     d.metadata_ready = scatter_first ? 1 : 0;
+    d.units_on_device = 0;
     // where each CTA's range [b*U/C, (b+1)*U/C) starts: (request, its first unit)
     d.has_table = d.num_ctas <= kDecodeTableCtas;
     if (d.has_table) {
@@ -147,6 +148,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
         pa.n_entries = 0;
         // the scatter, the decode kernel or an earlier prefill launch runs first
         pa.metadata_ready = (scatter_first || plan.fast_decode || l > 0) ? 1 : 0;
+        pa.device_work = 0;
         pa.total_ctas = 0;
         for (size_t i = (size_t)l * kPrefillMaxEntries;
              i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
@@ -168,6 +170,64 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   if (plan.fast_decode && plan.fast_prefill) plan.portable_mode = -1;
   else if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
   else if (plan.fast_prefill) plan.portable_mode = U > 0 ? 1 : -1;
+}
+
+bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_prefill,
+                     void* workspace, size_t workspace_bytes) {
+  plan.workspace = workspace;
+  plan.workspace_bytes = workspace_bytes;
+  plan.fast_decode = false;
+  plan.fast_prefill = false;
+  plan.n_prefill_launches = 0;
+  plan.portable_mode = -1;
+  if (a.dtype != CB_BF16) return false;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
+  const bool tile_pages_ok =
+      a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
+  if (!(a.block_size % 16 == 0 && G <= 8 && a.num_kv_heads % HB == 0)) return false;
+  if (!(tile_pages_ok && G <= 16 && kRowsPerTile % G == 0)) return false;
+
+  DecodeArgs& d = plan.decode;
+  d.a = a;
+  d.heads_per_cta = HB;
+  d.total_units = 0;  // summed by the kernel
+  d.units_on_device = 1;
+  d.num_ctas = std::min(sm_count(), kMaxDecodeCtas);
+  d.stage_bytes = 2 * (a.head_dim / 64) * HB * 16 * 128;
+  d.q_slot_bytes = HB * G * a.head_dim * 2;
+  const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
+  d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
+  d.metadata_ready = 0;
+  d.has_table = 0;
+  const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  d.counters = reinterpret_cast<int*>(ws + w.counters);
+  d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+  d.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
+  if (d.stages < 2) return false;
+  plan.fast_decode = with_decode;
+
+  PrefillArgs& pa = plan.prefill[0];
+  pa.a = a;
+  pa.tile_tokens = kRowsPerTile / G;
+  pa.box_keys = std::min(a.block_size, 128);
+  pa.n_entries = 0;
+  pa.metadata_ready = 0;
+  pa.device_work = 1;
+  pa.total_ctas = prefill_ctas_bound(a.num_tokens, a.num_requests, pa.tile_tokens,
+                                     a.num_kv_heads);
+  plan.n_prefill_launches = with_prefill ? 1 : 0;
+  plan.fast_prefill = with_prefill;
+  return true;
+}
+
+cudaError_t prepare_plan(const Plan& plan, const StepArgs& a) {
+  cudaError_t e = cudaSuccess;
+  if (plan.fast_decode) e = prepare_decode(plan.decode);
+  if (e == cudaSuccess && plan.fast_prefill) e = prepare_prefill(a.head_dim);
+  return e;
 }
 
 size_t workspace_extent(const Plan& plan, const StepArgs& a) {

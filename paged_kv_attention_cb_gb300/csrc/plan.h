@@ -35,6 +35,18 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream);
 
+// A plan whose launches depend only on the step's padded shape (a.num_requests,
+// a.num_tokens) and static sizes, for capture in a CUDA graph that is replayed for
+// every batch of that shape: the decode kernel sums its work on the device and the
+// prefill kernel finds its tiles in the device metadata. False when the shape
+// needs a kernel this mode does not cover (fp32, or a decode/prefill case only the
+// portable kernel runs). with_decode / with_prefill: whether the graph has the
+// decode / prefill launch (the batches it serves have rows of that kind).
+bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_prefill,
+                     void* workspace, size_t workspace_bytes);
+// Set the kernel attributes of the plan's launches (before a capture).
+cudaError_t prepare_plan(const Plan& plan, const StepArgs& a);
+
 // Bytes at the start of the workspace that the planned launch reads or writes
 // (the rest of a cb_workspace_size() buffer is headroom for larger plans), and
 // the leading part of it that must be zero before a call (error word, counters).

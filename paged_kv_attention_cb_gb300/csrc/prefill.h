@@ -27,14 +27,22 @@ struct PrefillArgs {
   int box_keys;      // keys per page box: min(block_size, 128)
   int n_entries;
   int metadata_ready;  // a libcb kernel precedes this one in the step: q and the metadata are visible
+  int device_work;     // entries unused: each CTA finds its work in the device metadata (graph
+                       // replays: nothing in the arguments depends on the batch); total_ctas is
+                       // then an upper bound and the CTAs past the step's work exit at once
   int total_ctas;    // sum over entries of prefill_ctas(n_qtiles, Hkv)
   PrefillEntry entries[kPrefillMaxEntries];  // heaviest first
 };
 
 size_t prefill_smem_bytes(int head_dim);
+// Most prefill CTAs a step of up to `num_tokens` query tokens in `num_requests`
+// requests can need (the grid of a launch whose work is found on the device).
+int prefill_ctas_bound(int num_tokens, int num_requests, int tile_tokens, int num_kv_heads);
 // CTAs the tile kernel runs for one request of n_qtiles query tiles.
 int prefill_ctas(int n_qtiles, int num_kv_heads);
 // Launch the tile kernel over the prefill requests listed in `p` (already sorted).
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream);
+// Kernel attributes the launch needs, set without launching (before a stream capture).
+cudaError_t prepare_prefill(int head_dim);
 
 }  // namespace cb

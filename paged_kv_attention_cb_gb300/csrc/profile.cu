@@ -60,6 +60,21 @@ void note_launch_end(KernelId id, cudaStream_t stream) {
   t_open_start = nullptr;
 }
 
+void note_replayed_launches(const long long* per_kernel) {
+  for (int k = 0; k < kNumKernels; ++k)
+    g_launches[k].fetch_add(per_kernel[k], std::memory_order_relaxed);
+}
+
+void launch_counts(long long* per_kernel) {
+  for (int k = 0; k < kNumKernels; ++k) per_kernel[k] = g_launches[k].load();
+}
+
+bool set_kernel_timing(bool enable) {
+  const bool was = t_timing;
+  t_timing = enable;
+  return was;
+}
+
 }  // namespace cb
 
 extern "C" {

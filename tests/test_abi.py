@@ -158,3 +158,44 @@ def test_ring_validation_accepts_exact_fit(lib):
     # 58..62, so a ring of 5 pages fits; 40 new tokens after 960 positions span 56..62
     assert call_ring(lib, qsl=[0, 0], seq=[1000], ring=5, window=64) == 0
     assert call_ring(lib, qsl=[0, 0], seq=[1000], ring=7, window=104) == 0
+
+
+# ------------------------------------------------------------------ CUDA-graph cache (host side)
+
+
+def test_graph_cache_lifecycle(lib):
+    h = ctypes.c_void_p()
+    assert lib.cb_graph_cache_create(64, 0, ctypes.byref(h)) == 0 and h.value
+    g, c, r = ctypes.c_int64(-1), ctypes.c_int64(-1), ctypes.c_int64(-1)
+    assert lib.cb_graph_cache_stats(h, ctypes.byref(g), ctypes.byref(c), ctypes.byref(r)) == 0
+    assert (g.value, c.value, r.value) == (0, 0, 0)
+    lib.cb_graph_cache_destroy(h)
+    bad = ctypes.c_void_p()
+    assert lib.cb_graph_cache_create(0, 0, ctypes.byref(bad)) == 1 and not bad.value
+    assert lib.cb_graph_cache_create(8, -1, ctypes.byref(bad)) == 1
+
+
+def call_graphed(lib, cache, qsl, seq, T, stream=FAKE, Hq=4, Hkv=2, D=64, BS=16):
+    qsl = np.ascontiguousarray(qsl, dtype=np.int32)
+    seq = np.ascontiguousarray(seq, dtype=np.int32)
+    R = len(seq)
+    stride = max(1, int(max((seq + BS - 1) // BS)))
+    return lib.cb_paged_attention_graphed(
+        cache, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, FAKE, stride,
+        qsl.ctypes.data_as(ctypes.c_void_p), seq.ctypes.data_as(ctypes.c_void_p), R, T, 40, BS,
+        Hq, Hkv, D, 0.0, 0, 1, 0, FAKE, lib.cb_workspace_size(R, T, Hq, Hkv, D), stream)
+
+
+def test_graphed_validation_rejects_before_any_launch(lib):
+    h = ctypes.c_void_p()
+    assert lib.cb_graph_cache_create(4, 0, ctypes.byref(h)) == 0
+    try:
+        assert call_graphed(lib, None, [0, 1, 2, 2, 2], [5, 9, 0, 0], T=4) == 1   # no cache
+        assert call_graphed(lib, h, [0, 1, 2, 2], [5, 9, 0], T=4) == 1            # R not padded
+        assert call_graphed(lib, h, [0, 1, 2, 2, 2], [5, 9, 0, 0], T=6) == 1      # T not padded
+        assert call_graphed(lib, h, [0, 1, 5, 5, 5], [5, 9, 0, 0], T=4) == 2      # qsl[R] > T
+        assert call_graphed(lib, h, [0, 1, 2, 2, 2], [5, 9, 0, 0], T=4, stream=None) == 1
+        g = ctypes.c_int64(-1)
+        assert lib.cb_graph_cache_stats(h, ctypes.byref(g), None, None) == 0 and g.value == 0
+    finally:
+        lib.cb_graph_cache_destroy(h)
