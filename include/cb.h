@@ -136,7 +136,10 @@ cb_status cb_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void
  * cb_workspace_size -- bytes of device workspace cb_paged_attention needs for
  * a step with these sizes (an upper bound; it does not depend on the lengths).
  * The workspace holds the device error word, per-request arrival counters and
- * the split-KV partial results.
+ * the split-KV partial results. One workspace serves every step of up to
+ * num_requests requests with the same num_q_heads / num_kv_heads / head_dim:
+ * its layout follows its size, not the step's request count, so steps of any
+ * smaller size can share it (one stream at a time).
  */
 size_t cb_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim);

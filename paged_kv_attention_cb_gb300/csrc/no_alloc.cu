@@ -85,7 +85,7 @@ extern "C" cb_status cb_paged_attention_no_alloc(
     cb::Plan plan;
     cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, scratch, bound);
     extent = cb::workspace_extent(plan, a);
-    zeroed = cb::workspace_zeroed_prefix(a);
+    zeroed = cb::workspace_zeroed_prefix(a, bound);
   }
   if (extent > kScratchBytes || zeroed > kScratchBytes)
     return cb::report_error(CB_ERR_WORKSPACE,

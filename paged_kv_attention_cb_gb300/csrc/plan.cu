@@ -48,6 +48,23 @@ WorkspaceLayout layout(int32_t R, int32_t Hq, int32_t Hkv, int32_t D) {
   return w;
 }
 
+// The layout of a workspace of `bytes`: that of the largest request count it holds,
+// not of the step's own count, so that every step on one workspace finds the arrival
+// counters, the partial (m, l) and the partial outputs at the same offsets. (The
+// counters must read zero at the start of a step; with offsets that moved with the
+// request count, a larger step's counters could land where a smaller step left
+// partials.) The estimate is conservative: layout(R).total <= bytes.
+WorkspaceLayout layout_of(size_t bytes, const StepArgs& a) {
+  const size_t Hq = (size_t)a.num_q_heads, D = (size_t)a.head_dim;
+  const size_t hg = (size_t)(std::max(a.num_kv_heads, 1) + kDecodeMaxHeads - 1) / kDecodeMaxHeads;
+  const size_t per_request = hg * 4 + Hq * 8 + Hq * D * 4;
+  const size_t fixed = kWorkspaceHeaderBytes + 512 + (size_t)kMaxDecodeCtas * (Hq * 8 + Hq * D * 4);
+  long long r = bytes > fixed ? (long long)((bytes - fixed) / per_request) : 0;
+  r = std::min<long long>(r, 1 << 24);
+  r = std::max<long long>(r, a.num_requests);  // the size check left room for the step's R
+  return layout((int32_t)r, a.num_q_heads, a.num_kv_heads, a.head_dim);
+}
+
 int decode_units_host(int seq, int window) {
   const int lo = window > 0 ? std::max(0, seq - window) : 0;
   return (seq - 1) / 16 - lo / 16 + 1;
@@ -116,7 +133,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
       }
       for (; b < d.num_ctas; ++b) d.cta_first[b] = make_int2(-1, 0);
     }
-    const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+    const WorkspaceLayout w = layout_of(workspace_bytes, a);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     d.counters = reinterpret_cast<int*>(ws + w.counters);
     d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
@@ -200,7 +217,7 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
   d.metadata_ready = 0;
   d.has_table = 0;
-  const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  const WorkspaceLayout w = layout_of(workspace_bytes, a);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   d.counters = reinterpret_cast<int*>(ws + w.counters);
   d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
@@ -232,13 +249,13 @@ cudaError_t prepare_plan(const Plan& plan, const StepArgs& a) {
 
 size_t workspace_extent(const Plan& plan, const StepArgs& a) {
   if (!plan.fast_decode) return kWorkspaceHeaderBytes;
-  const WorkspaceLayout w = layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  const WorkspaceLayout w = layout_of(plan.workspace_bytes, a);
   const size_t slots = (size_t)a.num_requests + (size_t)plan.decode.num_ctas;
   return w.part_o + slots * a.num_q_heads * (size_t)a.head_dim * 4;
 }
 
-size_t workspace_zeroed_prefix(const StepArgs& a) {
-  return layout(a.num_requests, a.num_q_heads, a.num_kv_heads, a.head_dim).part_ml;
+size_t workspace_zeroed_prefix(const StepArgs& a, size_t workspace_bytes) {
+  return layout_of(workspace_bytes, a).part_ml;
 }
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {

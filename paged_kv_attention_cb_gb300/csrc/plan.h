@@ -50,7 +50,9 @@ cudaError_t prepare_plan(const Plan& plan, const StepArgs& a);
 // Bytes at the start of the workspace that the planned launch reads or writes
 // (the rest of a cb_workspace_size() buffer is headroom for larger plans), and
 // the leading part of it that must be zero before a call (error word, counters).
+// The workspace's layout depends on its size only, never on the step's request
+// count, so that steps of any size can share one workspace.
 size_t workspace_extent(const Plan& plan, const StepArgs& a);
-size_t workspace_zeroed_prefix(const StepArgs& a);
+size_t workspace_zeroed_prefix(const StepArgs& a, size_t workspace_bytes);
 
 }  // namespace cb

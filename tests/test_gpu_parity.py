@@ -283,3 +283,32 @@ def test_long_decode_ring_full_size():
     spec = workloads.long_decode_ring()
     assert spec.ring_blocks == 256 and spec.block_table.shape[1] == 256  # window 4096 from 28672
     sampled_check(spec, n_rows=16)
+
+
+# ------------------------------------------------------------------ workspace reuse
+
+
+def test_workspace_reused_across_growing_request_counts():
+    """One workspace for a 40-request step with many split requests, then a 256-request
+    step: the larger step's split-merge counters must read zero, not where the smaller
+    step left partial results (the workspace layout follows its size, not the step)."""
+    ws = cb.alloc_workspace(256, 256, 32, 8, 128)
+    small = GpuStep(workloads.decode_step(seed=22, R=40, lo=4096, hi=8192))
+    small.ws = ws
+    small.run()
+    torch.cuda.synchronize()
+    big_spec = workloads.decode_step(seed=21, R=256, lo=1024, hi=6000)
+    big = GpuStep(big_spec)
+    big.ws = ws
+    h = big.host_inputs()
+    out = big.run()
+    torch.cuda.synchronize()
+    assert cb.read_error_word(ws) == 0
+    assert torch.isfinite(out.float()).all()
+    rows = sample_rows(big_spec, 16)
+    ref = oracle_step(big_spec, h, rows=rows)
+    compare(big_spec, out, ref, rows=rows)
+    # and back down: a small step after the large one on the same workspace
+    again = small.run()
+    torch.cuda.synchronize()
+    assert torch.isfinite(again.float()).all()

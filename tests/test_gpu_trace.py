@@ -72,3 +72,48 @@ def test_reduced_trace_all_steps(policy):
     assert n_steps > 20 and n_mixed >= (1 if policy == "prefill_first" else 5)
     if policy == "fifo_prefix_cache":
         assert n_aliased > 5
+
+
+def test_full_size_fifo_trace_sampled_rows():
+    """The whole FIFO trace (512 requests, 2157 steps, 65536 pages) through the C ABI with
+    the cache carried; the oracle follows with its own host cache and scatter and checks
+    sampled rows of 12 spread-out steps, then the whole cache bit for bit."""
+    cfg = TraceConfig()
+    steps = list(fifo_trace(cfg))
+    n = len(steps)
+    check_at = {int(k * (n - 1) / 11) for k in range(12)}
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg.seed)
+    shape = (cfg.num_pages, cfg.block_size, cfg.num_kv_heads, cfg.head_dim)
+    k_cache = torch.randn(*shape, generator=g, device="cuda").to(torch.bfloat16)
+    v_cache = torch.randn(*shape, generator=g, device="cuda").to(torch.bfloat16)
+    hk = k_cache.cpu().float().numpy()
+    hv = v_cache.cpu().float().numpy()
+    ws = cb.alloc_workspace(cfg.max_requests_per_batch, cfg.max_batch_tokens, cfg.num_q_heads,
+                            cfg.num_kv_heads, cfg.head_dim)
+    checked = 0
+    for i, st in enumerate(steps):
+        sp = st.spec
+        q, k_new, v_new = draw_step(sp)
+        md = {k: torch.from_numpy(getattr(sp, k).copy()).cuda()
+              for k in ("query_start_loc", "seq_lens", "block_table", "slot_mapping")}
+        out = torch.full_like(q, float("nan"))
+        cb.paged_attention(out, q, k_cache, v_cache, md["query_start_loc"], md["seq_lens"],
+                           md["block_table"], sp.query_start_loc, sp.seq_lens, ws, scale=sp.scale,
+                           k_new=k_new, v_new=v_new, slot_mapping=md["slot_mapping"])
+        oracle.scatter_kv(hk, hv, k_new.cpu().float().numpy(), v_new.cpu().float().numpy(),
+                          sp.slot_mapping)
+        if i in check_at:
+            rows = sorted(set(np.random.default_rng(i).integers(0, sp.T, size=24).tolist()))
+            ref = oracle.paged_attention(q.cpu().float().numpy(), hk, hv, sp.query_start_loc,
+                                         sp.seq_lens, sp.block_table, sp.block_size, sp.scale,
+                                         rows=rows)
+            got = out.cpu().float().numpy().astype(np.float64)
+            err = np.abs(got[rows] - ref[rows])
+            assert np.isfinite(got[rows]).all(), i
+            assert err.max() <= BF16_MAX_ABS and err.mean() <= BF16_MEAN_ABS, (i, err.max())
+            checked += 1
+    assert cb.read_error_word(ws) == 0
+    assert checked == len(check_at)
+    assert np.array_equal(k_cache.cpu().float().numpy()[2:], hk[2:])
+    assert np.array_equal(v_cache.cpu().float().numpy()[2:], hv[2:])
