@@ -839,7 +839,7 @@ def copy_main(args, world, rank, local):
                          "peak": peak, "unit": "GB/s", "frac": value / world / peak,
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": moved, "avg_launch_ms": ms,
-                         "traffic": None},
+                         "traffic": recorded_traffic("copy_blocks", conf["workload"])},
             "cpu_baseline": cpu, "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
 
