@@ -45,6 +45,7 @@ import json
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -120,7 +121,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+        # raw samples (the JSON line carries their summary); CB_BENCH_CLOCKS_DIR keeps them
+        self.path = os.path.join(os.environ.get("CB_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
