@@ -20,8 +20,9 @@
 //   directly, otherwise each segment writes an unnormalised partial
 //   (m, l, o) and a bookkeeping warp bumps the request's arrival counter off
 //   the streaming path; the CTA that delivers the last partial merges them
-//   (log-sum-exp) after its own stream and resets the counter, so no second
-//   kernel is needed.
+//   (log-sum-exp) after its own stream, pulling the partials into its idle
+//   stage ring with bulk copies, and resets the counter, so no second kernel
+//   is needed.
 // * GQA packing. One CTA covers up to 8 KV heads (one consumer warp each) and
 //   all G query heads of each KV head, so K/V are read once for the group.
 // * Staging. A producer warp moves each 16-key block of all the CTA's heads
@@ -71,6 +72,8 @@ struct DecodeSmem {
   uint64_t qempty[2];
   uint64_t done_full[kDoneRing];
   uint64_t merges_ready;
+  uint64_t ring_free;   // the stage ring may take a batch of partials (merges)
+  uint64_t merge_full;  // a batch of partials has landed
   SegDesc seg[2];
   SegDesc done[kDoneRing];
   long long scan[16];
@@ -87,16 +90,19 @@ CB_DEV int kb_lo_of(int seq, int window) {
   return lo / kKB;
 }
 
+// Key blocks a decode query of a request of seq_len `seq` attends.
+CB_DEV int units_of(int seq, int window) { return (seq - 1) / kKB - kb_lo_of(seq, window) + 1; }
+
 // Key blocks of request r if it is a decode request, else 0.
+// (The three loads are independent: one memory round trip.)
 CB_DEV int decode_units(const DecodeArgs& p, int r, int* seq_out, int* t_out) {
   const int q0 = __ldg(p.a.query_start_loc + r);
   const int q1 = __ldg(p.a.query_start_loc + r + 1);
-  if (q1 - q0 != 1) return 0;
   const int seq = __ldg(p.a.seq_lens + r);
-  if (seq <= 0) return 0;
   *seq_out = seq;
   *t_out = q0;
-  return (seq - 1) / kKB - kb_lo_of(seq, p.a.sliding_window) + 1;
+  if (q1 - q0 != 1 || seq <= 0) return 0;
+  return units_of(seq, p.a.sliding_window);
 }
 
 // CTA that owns global key block u (ranges [b*U/C, (b+1)*U/C)).
@@ -126,79 +132,96 @@ CB_DEV long long warp_incl_scan(long long v) {
   return v;
 }
 
-// Log-sum-exp merge of the nseg partials of request d.r for this warp's G
-// query heads: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s. With at
-// most 32 segments the statistics take one batch of loads (lane s holds
-// segment s) and the partial outputs are loaded several segments at a time,
-// so a merge costs a couple of L2 round trips.
+// Log-sum-exp merge of the nseg partials of request d.r, by the CTA's consumer
+// warps (warp hl: the G query heads of its KV head): out = sum_s 2^(m_s - M) o_s /
+// sum_s 2^(m_s - M) l_s. The stage ring is idle once the stream is over, so the
+// partial outputs come into it by 1-D bulk copies (as many segments per batch as it
+// holds), issued by one thread, while every lane loads the (m, l) of segment
+// s0 + lane: a batch costs one L2 round trip whatever its size. M is kept per batch
+// and the accumulator rescaled when a later batch raises it. ring_free (one arrival
+// per consumer warp) says the ring's last contents are consumed, merge_full that a
+// batch has landed; n_free / n_full count their completed phases.
 template <int D, int G>
-CB_DEV void merge_partials(const DecodeArgs& p, const SegDesc& d, int qh_base, int q_row_elems) {
-  constexpr int J = G * D / 32;        // output elements per lane
-  constexpr int SB = G <= 4 ? 4 : 2;   // segments loaded per batch
+CB_DEV bool merge_request(const DecodeArgs& p, const SegDesc& d, uint8_t* ring, int ring_bytes,
+                          uint64_t* ring_free, uint64_t* merge_full, int hl, int hg, int HB,
+                          int q_row_elems, uint32_t& n_free, uint32_t& n_full) {
+  constexpr int J = G * D / 32;  // outputs per lane: element j * 32 + lane of the warp's G x D
   const int lane = threadIdx.x & 31;
   const int Hq = p.a.num_q_heads;
-  const int nseg = d.nseg;
+  const int part_floats = HB * G * D;  // one segment's partial output for this CTA's heads
+  const int cap = min(32, ring_bytes / (part_floats * 4));
   const long long slot0 = (long long)d.r + d.b_first;
+  const int qh_cta = hg * HB * G;
+  const int qh_base = qh_cta + hl * G;
   float acc[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) acc[j] = 0.f;
   float M[G], L[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) M[h] = -FLT_MAX;
-  // running maximum over all segments (lane-parallel, 32 segments per pass)
-  for (int s0 = 0; s0 < nseg; s0 += 32) {
-    if (s0 + lane < nseg) {
-      const float2* ml = p.part_ml + (slot0 + s0 + lane) * Hq + qh_base;
-#pragma unroll
-      for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&ml[h].x));
-    }
-  }
-#pragma unroll
   for (int h = 0; h < G; ++h) {
-    M[h] = warp_max(M[h]);
+    M[h] = -FLT_MAX;
     L[h] = 0.f;
   }
-  for (int s0 = 0; s0 < nseg; s0 += 32) {
-    // weights of segments s0 + lane
-    float w[G];
-    if (s0 + lane < nseg) {
+  for (int s0 = 0; s0 < d.nseg; s0 += cap) {
+    const int n = min(cap, d.nseg - s0);
+    if (!mbar_wait_warp(ring_free, n_free & 1)) return false;
+    ++n_free;
+    if (hl == 0 && lane == 0) {
+      fence_proxy_async_all();
+      mbar_arrive_expect_tx(merge_full, (uint32_t)(n * part_floats * 4));
+      for (int i = 0; i < n; ++i)
+        bulk_load(ring + (size_t)i * part_floats * 4,
+                  p.part_o + ((slot0 + s0 + i) * Hq + qh_cta) * D, (uint32_t)(part_floats * 4),
+                  merge_full);
+    }
+    float m[G], l[G], w[G];
+    if (lane < n) {
       const float2* ml = p.part_ml + (slot0 + s0 + lane) * Hq + qh_base;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float2 v = __ldcg(&ml[h]);
-        w[h] = exp2f(v.x - M[h]);
-        L[h] += w[h] * v.y;
+        m[h] = v.x;
+        l[h] = v.y;
       }
     } else {
 #pragma unroll
-      for (int h = 0; h < G; ++h) w[h] = 0.f;
-    }
-    const int n = min(32, nseg - s0);
-    for (int k = 0; k < n; k += SB) {
-      float v[SB][J];
-#pragma unroll
-      for (int sb = 0; sb < SB; ++sb) {
-        const float* o = p.part_o + ((slot0 + s0 + k + sb) * Hq + qh_base) * D;
-#pragma unroll
-        for (int j = 0; j < J; ++j) v[sb][j] = k + sb < n ? __ldcg(o + j * 32 + lane) : 0.f;
-      }
-#pragma unroll
-      for (int sb = 0; sb < SB; ++sb) {
-        const int src = min(k + sb, 31);
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const float ws = __shfl_sync(0xffffffffu, w[(j * 32) / D], src);
-          acc[j] = fmaf(ws, v[sb][j], acc[j]);
-        }
+      for (int h = 0; h < G; ++h) {
+        m[h] = -FLT_MAX;
+        l[h] = 0.f;
       }
     }
+    float sc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float mn = fmaxf(M[h], warp_max(m[h]));
+      sc[h] = exp2f(M[h] - mn);  // 0 on the first batch (acc and L are 0 then)
+      M[h] = mn;
+      w[h] = lane < n ? exp2f(m[h] - mn) : 0.f;
+      L[h] = L[h] * sc[h] + warp_sum(w[h] * l[h]);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] *= sc[(j * 32) / D];
+    if (!mbar_wait_warp(merge_full, n_full & 1)) return false;
+    ++n_full;
+    const float* buf = reinterpret_cast<const float*>(ring) + hl * G * D;
+    for (int i = 0; i < n; ++i) {
+      float ws[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) ws[h] = __shfl_sync(0xffffffffu, w[h], i);
+      const float* src = buf + (size_t)i * part_floats;
+#pragma unroll
+      for (int j = 0; j < J; ++j) acc[j] = fmaf(ws[(j * 32) / D], src[j * 32 + lane], acc[j]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ring_free);
   }
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems +
                        qh_base * D;
 #pragma unroll
-  for (int h = 0; h < G; ++h) L[h] = 1.f / warp_sum(L[h]);
+  for (int h = 0; h < G; ++h) L[h] = 1.f / L[h];
 #pragma unroll
   for (int j = 0; j < J; ++j) out[j * 32 + lane] = __float2bfloat16_rn(acc[j] * L[(j * 32) / D]);
+  return true;
 }
 
 }  // namespace
@@ -240,6 +263,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     for (int s = 0; s < kDoneRing; ++s) mbar_init(&sm.done_full[s], HB * 32);
     mbar_init(&sm.merges_ready, 1);
+    mbar_init(&sm.ring_free, HB);
+    mbar_init(&sm.merge_full, 1);
     sm.first_r = -1;
     sm.first_u = 0;
     sm.abort_flag = 0;
@@ -287,8 +312,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // ---- this CTA's first request: from the host's table, or by a block scan
   if (p.has_table) {
     if (threadIdx.x == 0) {
-      sm.first_r = p.cta_first[b].x;
-      sm.first_u = p.cta_first[b].y;
+      sm.first_r = p.cta_first[b].r;
+      sm.first_u = p.cta_first[b].u_r;
     }
     __syncthreads();
   } else if (u_lo < u_hi) {
@@ -363,11 +388,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // walk state of the current segment
     int r = -1, seq = 0, t = 0, units = 0;
     long long u_r = 0, u = u_lo;
-    if (u_lo < u_hi && sm.first_r >= 0) {
-      r = sm.first_r;
-      u_r = sm.first_u;
-      load_window(r);
-    }
     auto fetch = [&](int rr) {
       const int j = rr - wbase;
       units = __shfl_sync(0xffffffffu, w_units, j);
@@ -376,12 +396,28 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     };
     int kb0 = 0, kb1 = 0;
     int pages = 0;  // page ids of the batch about to be issued (lane j: key block kb + j)
-    if (r >= 0) {
-      fetch(r);
-      const int kbl = kb_lo_of(seq, p.a.sliding_window);
-      kb0 = kbl + (int)(u - u_r);
-      kb1 = kbl + (int)(min(u_r + units, u_hi) - u_r);
-      pages = load_pages(r, kb0, min(32, kb1 - kb0));
+    if (u_lo < u_hi && sm.first_r >= 0) {
+      r = sm.first_r;
+      u_r = sm.first_u;
+      if (p.has_table) {
+        // the host placed the first segment: the first copies wait only on its page
+        // ids; the window of following requests is needed at the first switch
+        const DecodeCtaStart& c = p.cta_first[b];
+        kb0 = c.kb0;
+        kb1 = c.kb1;
+        t = c.t;
+        seq = c.seq;
+        units = units_of(seq, p.a.sliding_window);
+        pages = load_pages(r, kb0, min(32, kb1 - kb0));
+        load_window(r);
+      } else {
+        load_window(r);
+        fetch(r);
+        const int kbl = kb_lo_of(seq, p.a.sliding_window);
+        kb0 = kbl + (int)(u - u_r);
+        kb1 = kbl + (int)(min(u_r + units, u_hi) - u_r);
+        pages = load_pages(r, kb0, min(32, kb1 - kb0));
+      }
     }
     if (p.metadata_ready) grid_dependency_wait();  // the scatter must be complete
     while (r >= 0 && ok) {
@@ -408,28 +444,20 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   &sm.qfull[qs]);
       }
       __syncwarp();
-      // the segment after this one (to prefetch its first page ids)
-      int nr = -1, nkb0 = 0, nkb1 = 0;
-      long long nu_r = u_r + units;
-      if (seg_u1 < u_hi) {
-        nr = next_decode(r + 1);
-        if (nr >= R) nr = -1;
-      }
+      // the segment after this one (looked up once this segment's first copy is out)
+      int nr = -2, nkb0 = 0, nkb1 = 0;
+      const long long nu_r = u_r + units;
+      auto lookup_next = [&]() {
+        if (nr != -2) return;
+        nr = -1;
+        if (seg_u1 < u_hi) {
+          nr = next_decode(r + 1);
+          if (nr >= R) nr = -1;
+        }
+      };
       for (int kb_base = kb0; kb_base < kb1 && ok; kb_base += 32) {
         const int nkb = min(32, kb1 - kb_base);
         const int cur = pages;
-        // the batch after this one: rest of this segment, or the next segment's start
-        if (kb_base + 32 < kb1) {
-          pages = load_pages(r, kb_base + 32, min(32, kb1 - kb_base - 32));
-        } else if (nr >= 0) {
-          const int j = nr - wbase;
-          const int n_units = __shfl_sync(0xffffffffu, w_units, j);
-          const int n_seq = __shfl_sync(0xffffffffu, w_seq, j);
-          const int nkbl = kb_lo_of(n_seq, p.a.sliding_window);
-          nkb0 = nkbl;
-          nkb1 = nkbl + (int)(min(nu_r + n_units, u_hi) - nu_r);
-          pages = load_pages(nr, nkb0, min(32, nkb1 - nkb0));
-        }
         for (int j = 0; j < nkb; ++j) {
           const int pg = __shfl_sync(0xffffffffu, cur, j);
           const int kb = kb_base + j;
@@ -457,9 +485,29 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           }
           __syncwarp();
           ++i;
+          if (j == 0) {
+            // page ids of the batch after this one: the rest of this segment, or the
+            // next segment's start
+            if (kb_base + 32 < kb1) {
+              pages = load_pages(r, kb_base + 32, min(32, kb1 - kb_base - 32));
+            } else {
+              lookup_next();
+              if (nr >= 0) {
+                const int jn = nr - wbase;
+                const int n_units = __shfl_sync(0xffffffffu, w_units, jn);
+                const int n_seq = __shfl_sync(0xffffffffu, w_seq, jn);
+                const int nkbl = kb_lo_of(n_seq, p.a.sliding_window);
+                nkb0 = nkbl;
+                nkb1 = nkbl + (int)(min(nu_r + n_units, u_hi) - nu_r);
+                pages = load_pages(nr, nkb0, min(32, nkb1 - nkb0));
+              }
+            }
+          }
         }
       }
       ++k;
+      if (!ok) break;
+      lookup_next();
       if (nr < 0) break;
       // advance to the next segment
       r = nr;
@@ -504,11 +552,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       const SegDesc dd = sm.done[nd];
       if (dd.r < 0) break;
-      __threadfence();
       int last = 0;
       if (lane == 0) {
+        // release: the consumers' partial stores (synchronised with this thread by
+        // done_full) precede the count; acquire: the last adder sees every partial
         int* cnt = p.counters + (long long)dd.r * gridDim.y + hg;
-        const int old = atomicAdd(cnt, 1);
+        const int old = atomic_add_acq_rel_gpu(cnt, 1);
         last = old == dd.nseg - 1;
         if (last) *cnt = 0;  // every segment has arrived: ready for the next step
       }
@@ -518,7 +567,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         ++npend;
       }
     }
-    __threadfence();
     if (lane == 0) {
       sm.npend = npend;
       mbar_arrive(&sm.merges_ready);
@@ -711,10 +759,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     return;
   }
   const int npend = *reinterpret_cast<volatile int*>(&sm.npend);
+  if (npend == 0) return;
+  // this warp is done with the stage ring (the merges reuse it)
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sm.ring_free);
+  uint32_t n_free = 0, n_full = 0;
   for (int j = 0; j < npend; ++j) {
     const SegDesc d = sm.done[sm.pend[j]];
-    __threadfence();
-    merge_partials<D, G>(p, d, (hg * HB + hl) * G, q_row_elems);
+    if (!merge_request<D, G>(p, d, stages, p.stages * p.stage_bytes, &sm.ring_free,
+                             &sm.merge_full, hl, hg, HB, q_row_elems, n_free, n_full)) {
+      if (lane == 0) record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+      return;
+    }
   }
 }
 

@@ -14,6 +14,17 @@ constexpr int kDecodeTableCtas = 256;       // CTAs whose start is passed in the
 constexpr int CB_DEVERR_BLOCK_ID_CODE = 0x1;
 constexpr int CB_DEVERR_TIMEOUT_CODE = 0x4;
 
+// Where CTA b's range of key blocks starts, placed by the host from its mirrors of
+// the metadata, so that the CTA's first copies wait on one load (its page ids).
+struct DecodeCtaStart {
+  int r;    // first request (-1: none)
+  int u_r;  // global index of that request's first key block
+  int kb0;  // first key block (within the request) of the CTA's first segment
+  int kb1;  // one past its last key block
+  int t;    // packed query row of the request
+  int seq;  // its seq_len
+};
+
 struct DecodeArgs {
   StepArgs a;
   long long total_units;  // key blocks of all decode requests
@@ -29,7 +40,7 @@ struct DecodeArgs {
   float2* part_ml;        // [slots][Hq] (running max in log2 units, sum)
   int* counters;          // [R][head groups] arrivals of split requests (zero between steps)
   int has_table;          // cta_first is filled (num_ctas <= kDecodeTableCtas)
-  int2 cta_first[kDecodeTableCtas];  // per CTA: (first request, its first key-block index)
+  DecodeCtaStart cta_first[kDecodeTableCtas];
 };
 
 struct DecodePlan {

@@ -65,10 +65,10 @@ WorkspaceLayout layout_of(size_t bytes, const StepArgs& a) {
   return layout((int32_t)r, a.num_q_heads, a.num_kv_heads, a.head_dim);
 }
 
-int decode_units_host(int seq, int window) {
-  const int lo = window > 0 ? std::max(0, seq - window) : 0;
-  return (seq - 1) / 16 - lo / 16 + 1;
-}
+// First key block (16 keys) a decode query attends, and the number of blocks it attends.
+int kb_lo_host(int seq, int window) { return (window > 0 ? std::max(0, seq - window) : 0) / 16; }
+
+int decode_units_host(int seq, int window) { return (seq - 1) / 16 - kb_lo_host(seq, window) + 1; }
 
 }  // namespace
 
@@ -125,13 +125,17 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
         const int ql = h_qsl[r + 1] - h_qsl[r];
         if (ql != 1 || h_seq_lens[r] <= 0) continue;
         const int units = decode_units_host(h_seq_lens[r], a.sliding_window);
+        const int kbl = kb_lo_host(h_seq_lens[r], a.sliding_window);
         while (b < d.num_ctas && (long long)b * U / C < u + units) {
-          d.cta_first[b] = make_int2(r, (int)u);
+          const long long lo = (long long)b * U / C, hi = (long long)(b + 1) * U / C;
+          d.cta_first[b] = DecodeCtaStart{r, (int)u, kbl + (int)(lo - u),
+                                          kbl + (int)(std::min(u + units, hi) - u), h_qsl[r],
+                                          h_seq_lens[r]};
           ++b;
         }
         u += units;
       }
-      for (; b < d.num_ctas; ++b) d.cta_first[b] = make_int2(-1, 0);
+      for (; b < d.num_ctas; ++b) d.cta_first[b] = DecodeCtaStart{-1, 0, 0, 0, 0, 0};
     }
     const WorkspaceLayout w = layout_of(workspace_bytes, a);
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -67,6 +67,18 @@ CB_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Atomic add at GPU scope with acquire-release semantics: the writes this thread has
+// made or observed are visible to a thread that sees the new value, and this thread
+// sees the writes released by the adders before it.
+CB_DEV int atomic_add_acq_rel_gpu(int* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(reinterpret_cast<uint64_t>(ptr)), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------ TMA
 
 CB_DEV void prefetch_tensormap(const CUtensorMap* m) {
@@ -231,6 +243,13 @@ CB_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "
 CB_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Order the memory accesses this thread has made or observed through the generic
+// proxy (its own, and other threads' that it has acquired), in global and shared
+// memory, before the async-proxy copies it issues next: bulk copies that read
+// partials other CTAs stored, into shared memory that warps of this CTA last read
+// and wrote with ordinary instructions.
+CB_DEV void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero; relative
 // error ~2^-22, below the bf16 rounding that follows; 2^-inf = 0).
