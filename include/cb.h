@@ -135,8 +135,7 @@ cb_status cb_copy_blocks(const void* k_src, const void* v_src, void* k_dst, void
 /*
  * cb_workspace_size -- bytes of device workspace cb_paged_attention needs for
  * a step with these sizes (an upper bound; it does not depend on the lengths).
- * The workspace holds the device error word, per-request arrival counters and
- * the split-KV partial results. One workspace serves every step of up to
+ * The workspace holds the device error word and the split-KV partial results. One workspace serves every step of up to
  * num_requests requests with the same num_q_heads / num_kv_heads / head_dim:
  * its layout follows its size, not the step's request count, so steps of any
  * smaller size can share it (one stream at a time).
@@ -147,8 +146,7 @@ size_t cb_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_q
 /*
  * cb_workspace_init -- zero the whole workspace (asynchronously on `stream`).
  * Call once after allocating a workspace, and again after a call recorded
- * CB_DEVERR_TIMEOUT. Between calls the library leaves the workspace's
- * counters at zero itself; cb_read_error_word clears the error word.
+ * CB_DEVERR_TIMEOUT; cb_read_error_word clears the error word.
  */
 cb_status cb_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
@@ -307,8 +305,8 @@ cb_status cb_read_error_word(void* workspace, int32_t* h_error, void* stream);
  * The first call on a device looks up the array's device address with that
  * device current and caches it; make that first call before any stream
  * capture. Every call shares the one array and finds it holding the previous
- * call's contents; the call clears the part that must start at zero (error
- * word, split-request counters) on `stream` before its kernels. Calls whose
+ * call's contents; the call clears the part that must start at zero (the error
+ * word) on `stream` before its kernels. Calls whose
  * work overlaps on the GPU (other streams, other host threads) race on the
  * array: order them on one stream. The device error word lives in the array,
  * so cb_read_error_word cannot read it for these calls.

@@ -14,15 +14,14 @@
 //   all KV heads) are numbered in request order, u = 0 .. U-1, and CTA b of C
 //   takes the contiguous range [b*U/C, (b+1)*U/C): every CTA streams the same
 //   number of bytes whatever the length mix, and a long request is split
-//   across CTAs (split-KV). Each CTA finds its first request with a block scan
-//   over the decode lengths, then walks forward. A piece of a request inside
-//   one CTA is a segment; a request that lies in one CTA writes its output
-//   directly, otherwise each segment writes an unnormalised partial
-//   (m, l, o) and a bookkeeping warp bumps the request's arrival counter off
-//   the streaming path; the CTA that delivers the last partial merges them
-//   (log-sum-exp) after its own stream, pulling the partials into its idle
-//   stage ring with bulk copies, and resets the counter, so no second kernel
-//   is needed.
+//   across CTAs (split-KV). The host places each CTA's start (or, for a
+//   captured graph, each CTA finds it with a block scan over the decode
+//   lengths); the CTA then walks forward. A piece of a request inside one CTA
+//   is a segment; a request that lies in one CTA writes its output directly,
+//   otherwise each segment writes an unnormalised partial (m, l, o), and the
+//   combine kernel that follows on the stream merges them (log-sum-exp), one
+//   CTA per (split request, KV head), so a long request's merge is spread
+//   over several SMs instead of falling on the one that finishes last.
 // * GQA packing. One CTA covers up to 8 KV heads (one consumer warp each) and
 //   all G query heads of each KV head, so K/V are read once for the group.
 // * Staging. A producer warp moves each 16-key block of all the CTA's heads
@@ -59,27 +58,16 @@ struct SegDesc {
   int hi;      // last attended key (= seq_len - 1)
   int slot;    // partial slot (r + CTA index)
   int direct;  // 1: the request lies wholly in this CTA
-  int b_first; // first CTA of the request
-  int nseg;    // number of CTAs (segments) of the request
 };
-
-constexpr int kDoneRing = 4;  // split segments handed to the bookkeeping warp (<= 2) + end mark
 
 struct DecodeSmem {
   uint64_t full[kDecodeMaxStages];
   uint64_t empty[kDecodeMaxStages];
   uint64_t qfull[2];
   uint64_t qempty[2];
-  uint64_t done_full[kDoneRing];
-  uint64_t merges_ready;
-  uint64_t ring_free;   // the stage ring may take a batch of partials (merges)
-  uint64_t merge_full;  // a batch of partials has landed
   SegDesc seg[2];
-  SegDesc done[kDoneRing];
   long long scan[16];
   long long total_u;
-  int pend[kDoneRing];
-  int npend;
   int first_r;
   long long first_u;
   int abort_flag;
@@ -95,31 +83,19 @@ CB_DEV int units_of(int seq, int window) { return (seq - 1) / kKB - kb_lo_of(seq
 
 // Key blocks of request r if it is a decode request, else 0.
 // (The three loads are independent: one memory round trip.)
-CB_DEV int decode_units(const DecodeArgs& p, int r, int* seq_out, int* t_out) {
-  const int q0 = __ldg(p.a.query_start_loc + r);
-  const int q1 = __ldg(p.a.query_start_loc + r + 1);
-  const int seq = __ldg(p.a.seq_lens + r);
+CB_DEV int decode_units(const StepArgs& a, int r, int* seq_out, int* t_out) {
+  const int q0 = __ldg(a.query_start_loc + r);
+  const int q1 = __ldg(a.query_start_loc + r + 1);
+  const int seq = __ldg(a.seq_lens + r);
   *seq_out = seq;
   *t_out = q0;
   if (q1 - q0 != 1 || seq <= 0) return 0;
-  return units_of(seq, p.a.sliding_window);
+  return units_of(seq, a.sliding_window);
 }
 
 // CTA that owns global key block u (ranges [b*U/C, (b+1)*U/C)).
 CB_DEV int cta_of(long long u, long long U, int C) {
   return (int)(((u + 1) * (long long)C + U - 1) / U) - 1;
-}
-
-CB_DEV float warp_max(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
-CB_DEV float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
 }
 
 CB_DEV long long warp_incl_scan(long long v) {
@@ -132,102 +108,10 @@ CB_DEV long long warp_incl_scan(long long v) {
   return v;
 }
 
-// Log-sum-exp merge of the nseg partials of request d.r, by the CTA's consumer
-// warps (warp hl: the G query heads of its KV head): out = sum_s 2^(m_s - M) o_s /
-// sum_s 2^(m_s - M) l_s. The stage ring is idle once the stream is over, so the
-// partial outputs come into it by 1-D bulk copies (as many segments per batch as it
-// holds), issued by one thread, while every lane loads the (m, l) of segment
-// s0 + lane: a batch costs one L2 round trip whatever its size. M is kept per batch
-// and the accumulator rescaled when a later batch raises it. ring_free (one arrival
-// per consumer warp) says the ring's last contents are consumed, merge_full that a
-// batch has landed; n_free / n_full count their completed phases.
-template <int D, int G>
-CB_DEV bool merge_request(const DecodeArgs& p, const SegDesc& d, uint8_t* ring, int ring_bytes,
-                          uint64_t* ring_free, uint64_t* merge_full, int hl, int hg, int HB,
-                          int q_row_elems, uint32_t& n_free, uint32_t& n_full) {
-  constexpr int J = G * D / 32;  // outputs per lane: element j * 32 + lane of the warp's G x D
-  const int lane = threadIdx.x & 31;
-  const int Hq = p.a.num_q_heads;
-  const int part_floats = HB * G * D;  // one segment's partial output for this CTA's heads
-  const int cap = min(32, ring_bytes / (part_floats * 4));
-  const long long slot0 = (long long)d.r + d.b_first;
-  const int qh_cta = hg * HB * G;
-  const int qh_base = qh_cta + hl * G;
-  float acc[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) acc[j] = 0.f;
-  float M[G], L[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    M[h] = -FLT_MAX;
-    L[h] = 0.f;
-  }
-  for (int s0 = 0; s0 < d.nseg; s0 += cap) {
-    const int n = min(cap, d.nseg - s0);
-    if (!mbar_wait_warp(ring_free, n_free & 1)) return false;
-    ++n_free;
-    if (hl == 0 && lane == 0) {
-      fence_proxy_async_all();
-      mbar_arrive_expect_tx(merge_full, (uint32_t)(n * part_floats * 4));
-      for (int i = 0; i < n; ++i)
-        bulk_load(ring + (size_t)i * part_floats * 4,
-                  p.part_o + ((slot0 + s0 + i) * Hq + qh_cta) * D, (uint32_t)(part_floats * 4),
-                  merge_full);
-    }
-    float m[G], l[G], w[G];
-    if (lane < n) {
-      const float2* ml = p.part_ml + (slot0 + s0 + lane) * Hq + qh_base;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float2 v = __ldcg(&ml[h]);
-        m[h] = v.x;
-        l[h] = v.y;
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        m[h] = -FLT_MAX;
-        l[h] = 0.f;
-      }
-    }
-    float sc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float mn = fmaxf(M[h], warp_max(m[h]));
-      sc[h] = exp2f(M[h] - mn);  // 0 on the first batch (acc and L are 0 then)
-      M[h] = mn;
-      w[h] = lane < n ? exp2f(m[h] - mn) : 0.f;
-      L[h] = L[h] * sc[h] + warp_sum(w[h] * l[h]);
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j) acc[j] *= sc[(j * 32) / D];
-    if (!mbar_wait_warp(merge_full, n_full & 1)) return false;
-    ++n_full;
-    const float* buf = reinterpret_cast<const float*>(ring) + hl * G * D;
-    for (int i = 0; i < n; ++i) {
-      float ws[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) ws[h] = __shfl_sync(0xffffffffu, w[h], i);
-      const float* src = buf + (size_t)i * part_floats;
-#pragma unroll
-      for (int j = 0; j < J; ++j) acc[j] = fmaf(ws[(j * 32) / D], src[j * 32 + lane], acc[j]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ring_free);
-  }
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems +
-                       qh_base * D;
-#pragma unroll
-  for (int h = 0; h < G; ++h) L[h] = 1.f / L[h];
-#pragma unroll
-  for (int j = 0; j < J; ++j) out[j * 32 + lane] = __float2bfloat16_rn(acc[j] * L[(j * 32) / D]);
-  return true;
-}
-
 }  // namespace
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeMaxHeads * 32 + 64, 1)
+__global__ void __launch_bounds__(kDecodeMaxHeads * 32 + 32, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs p) {
   static_assert(D == 64 || D == 128, "head_dim");
@@ -261,14 +145,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       mbar_init(&sm.qfull[s], 1);
       mbar_init(&sm.qempty[s], HB);
     }
-    for (int s = 0; s < kDoneRing; ++s) mbar_init(&sm.done_full[s], HB * 32);
-    mbar_init(&sm.merges_ready, 1);
-    mbar_init(&sm.ring_free, HB);
-    mbar_init(&sm.merge_full, 1);
     sm.first_r = -1;
     sm.first_u = 0;
     sm.abort_flag = 0;
-    sm.npend = 0;
     fence_barrier_init();
   }
   if (warp == HB && lane == 0) {
@@ -287,7 +166,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     long long part = 0;
     for (int r = threadIdx.x; r < R; r += nthreads) {
       int seq = 0, t = 0;
-      part += decode_units(p, r, &seq, &t);
+      part += decode_units(p.a, r, &seq, &t);
     }
     part = warp_incl_scan(part);
     if (lane == 31) sm.scan[warp] = part;
@@ -321,7 +200,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int base_r = 0; base_r < R; base_r += nthreads) {
       const int r = base_r + threadIdx.x;
       int seq = 0, t = 0, units = 0;
-      if (r < R) units = decode_units(p, r, &seq, &t);
+      if (r < R) units = decode_units(p.a, r, &seq, &t);
       long long v = warp_incl_scan(units);
       if (lane == 31) sm.scan[warp] = v;
       __syncthreads();
@@ -357,13 +236,16 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // the TMA issue on global-memory latency.
     int k = 0;        // segments published
     long long i = 0;  // stages issued
+    // the KV stream is read once: it leaves L2 first, ahead of the partials that
+    // the combine kernel reads back
+    const uint64_t kv_policy = l2_policy_evict_first();
     bool ok = true;
     int wbase = -1, w_units = 0, w_seq = 0, w_t = 0;
     auto load_window = [&](int r0) {
       wbase = r0;
       const int r = r0 + lane;
       int seq = 0, t = 0, units = 0;
-      if (r < R) units = decode_units(p, r, &seq, &t);
+      if (r < R) units = decode_units(p.a, r, &seq, &t);
       w_units = units;
       w_seq = seq;
       w_t = t;
@@ -436,8 +318,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         d.hi = seq - 1;
         d.slot = r + b;
         d.direct = (b_first == b_last);
-        d.b_first = b_first;
-        d.nseg = b_last - b_first + 1;
         mbar_arrive_expect_tx(&sm.qfull[qs], q_bytes);
         bulk_load(qring + qs * p.q_slot_bytes,
                   q + (long long)t * q_row_elems + (long long)hg * HB * G * D, q_bytes,
@@ -478,9 +358,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             mbar_arrive_expect_tx(&sm.full[s], (uint32_t)p.stage_bytes);
 #pragma unroll
             for (int h = 0; h < kHalves; ++h) {
-              tma_load_4d(st + h * box_bytes, &tmap_k, &sm.full[s], h * 64, key0, hg * HB, pgc);
-              tma_load_4d(st + (kHalves + h) * box_bytes, &tmap_v, &sm.full[s], h * 64, key0,
-                          hg * HB, pgc);
+              tma_load_4d_hint(st + h * box_bytes, &tmap_k, &sm.full[s], h * 64, key0, hg * HB,
+                               pgc, kv_policy);
+              tma_load_4d_hint(st + (kHalves + h) * box_bytes, &tmap_v, &sm.full[s], h * 64,
+                               key0, hg * HB, pgc, kv_policy);
             }
           }
           __syncwarp();
@@ -539,47 +420,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     return;
   }
 
-  if (warp == HB + 1) {
-    // =================================================== arrival bookkeeping
-    // For every segment whose request spans several CTAs: make its partials
-    // visible device-wide, count its arrival, and remember the requests whose
-    // last partial this CTA delivered (merged by the consumers at the end).
-    int nd = 0, npend = 0;
-    for (;; ++nd) {
-      if (nd >= kDoneRing || !mbar_wait_warp(&sm.done_full[nd], 0)) {
-        if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
-        break;
-      }
-      const SegDesc dd = sm.done[nd];
-      if (dd.r < 0) break;
-      int last = 0;
-      if (lane == 0) {
-        // release: the consumers' partial stores (synchronised with this thread by
-        // done_full) precede the count; acquire: the last adder sees every partial
-        int* cnt = p.counters + (long long)dd.r * gridDim.y + hg;
-        const int old = atomic_add_acq_rel_gpu(cnt, 1);
-        last = old == dd.nseg - 1;
-        if (last) *cnt = 0;  // every segment has arrived: ready for the next step
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        if (lane == 0) sm.pend[npend] = nd;
-        ++npend;
-      }
-    }
-    if (lane == 0) {
-      sm.npend = npend;
-      mbar_arrive(&sm.merges_ready);
-    }
-    return;
-  }
-
   // ===================================================== consumer warps
   const int hl = warp;  // local KV head
   const int gid = lane >> 2;
   const int tq = lane & 3;
   const float sl2 = p.a.scale_log2;
-  int nd = 0;  // segments handed to the bookkeeping warp
   long long i = 0;
   for (int k = 0;; ++k) {
     const int qs = k & 1;
@@ -737,41 +582,135 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (h0 < G) pml[qh_base + h0] = make_float2(m0, l0);
         if (h1 < G) pml[qh_base + h1] = make_float2(m1, l1);
       }
-      // hand the segment to the bookkeeping warp (at most two per CTA: only
-      // a CTA's first and last segments can belong to a split request)
-      if (nd < kDoneRing - 1) {
-        if (hl == 0 && lane == 0) sm.done[nd] = d;
-        mbar_arrive(&sm.done_full[nd]);
-      } else if (lane == 0) {
-        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+    }
+  }
+}
+
+// Combine of the split decode requests: out = sum_s 2^(m_s - M) o_s /
+// sum_s 2^(m_s - M) l_s over the request's segments s (M = max_s m_s), the
+// log-sum-exp merge of split-KV partials. CTA (x, y) takes request x of the
+// host's list (or, with no list, request x itself, found split or not by the
+// same partition arithmetic as the decode grid) and KV heads
+// [y * kv_per_cta, (y + 1) * kv_per_cta): one thread per four consecutive
+// outputs, the partials of up to twelve segments in flight per thread. The host
+// sizes the grid to about one CTA per SM, so a request split over ten CTAs is
+// merged on several SMs at once. The kernel is launched right after the decode
+// kernel and waits for it on the device (programmatic dependent launch), with
+// its list entry or scan already done.
+template <int D, int G>
+__global__ void __launch_bounds__(kCombineMaxThreads)
+decode_combine_kernel(const CombineArgs c) {
+  constexpr int kChunk = 12;  // segments whose loads are in flight together
+  __shared__ long long red[32];
+  __shared__ long long totals[2];
+  const int x = blockIdx.x;
+  const int kvh0 = blockIdx.y * c.kv_per_cta;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nthreads = blockDim.x;
+  allow_dependent_launch();
+  int r, t, b_first, nseg;
+  if (c.n_entries >= 0) {
+    if (x >= c.n_entries) return;
+    const CombineEntry e = c.entries[x];
+    r = e.r;
+    t = e.t;
+    b_first = e.b_first;
+    nseg = e.nseg;
+  } else {
+    // the decode grid's partition from the device metadata: U (all decode key
+    // blocks), the key blocks of the requests before x, and C (CTAs in use)
+    const StepArgs& a = c.a;
+    r = x;
+    if (r >= a.num_requests) return;
+    long long all = 0, before = 0;
+    for (int i = threadIdx.x; i < a.num_requests; i += nthreads) {
+      int sq = 0, tt = 0;
+      const int u = decode_units(a, i, &sq, &tt);
+      all += u;
+      if (i < r) before += u;
+    }
+    for (int k = 0; k < 2; ++k) {
+      long long v = k == 0 ? all : before;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) red[warp] = v;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        long long tot = 0;
+        for (int w = 0; w < (nthreads >> 5); ++w) tot += red[w];
+        totals[k] = tot;
       }
-      ++nd;
+      __syncthreads();
+    }
+    int seq = 0;
+    const int units = decode_units(a, r, &seq, &t);
+    const long long U = totals[0];
+    if (units == 0 || U == 0) return;
+    const int C = U < (long long)c.num_ctas ? (int)U : c.num_ctas;
+    b_first = cta_of(totals[1], U, C);
+    nseg = cta_of(totals[1] + units - 1, U, C) - b_first + 1;
+    if (nseg < 2) return;  // written directly by its CTA
+  }
+  const int f = threadIdx.x;  // float4 f of the slice: outputs 4f .. 4f + 3
+  if (f >= c.kv_per_cta * G * D / 4) return;
+  const int Hq = c.a.num_q_heads;
+  const int qh = kvh0 * G + (4 * f) / D;
+  const long long slot0 = (long long)r + b_first;
+  const int o_off = kvh0 * G * D / 4 + f;  // float4 index within a slot
+  // segment s: ml_base[s * Hq], o_base[s * o_stride]
+  const float2* ml_base = c.part_ml + slot0 * Hq + qh;
+  const float4* o_base = reinterpret_cast<const float4*>(c.part_o + slot0 * Hq * D) + o_off;
+  const int o_stride = Hq * D / 4;
+  // the partials of CTAs that finished early may have left L2: ask for them while
+  // the decode grid drains (a hint; the values are read after the wait)
+  for (int i = 0; i < nseg; ++i) {
+    if ((4 * f) % D == 0) prefetch_l2(ml_base + i * Hq);
+    if (f % 8 == 0) prefetch_l2(o_base + (long long)i * o_stride);
+  }
+  grid_dependency_wait();  // the partials of the decode grid
+  float M = -FLT_MAX, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nseg; s0 += kChunk) {
+    const int n = min(kChunk, nseg - s0);
+    float2 ml[kChunk];
+    float4 o[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      if (i < n) {
+        ml[i] = __ldcg(ml_base + (s0 + i) * Hq);
+        o[i] = __ldcg(o_base + (long long)(s0 + i) * o_stride);
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+      if (i < n) mb = fmaxf(mb, ml[i].x);
+    const float sc = exp2f(M - mb);  // 0 on the first chunk (acc and L are 0 then)
+    M = mb;
+    L *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      if (i < n) {
+        const float w = exp2f(ml[i].x - mb);
+        L = fmaf(w, ml[i].y, L);
+        acc.x = fmaf(w, o[i].x, acc.x);
+        acc.y = fmaf(w, o[i].y, acc.y);
+        acc.z = fmaf(w, o[i].z, acc.z);
+        acc.w = fmaf(w, o[i].w, acc.w);
+      }
     }
   }
-  // ---- end of the stream: close the hand-off ring, then merge the requests
-  // whose last partial this CTA delivered
-  if (nd < kDoneRing) {
-    if (hl == 0 && lane == 0) sm.done[nd].r = -1;
-    mbar_arrive(&sm.done_full[nd]);
-  }
-  if (!mbar_wait_warp(&sm.merges_ready, 0)) {
-    if (lane == 0) record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
-    return;
-  }
-  const int npend = *reinterpret_cast<volatile int*>(&sm.npend);
-  if (npend == 0) return;
-  // this warp is done with the stage ring (the merges reuse it)
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&sm.ring_free);
-  uint32_t n_free = 0, n_full = 0;
-  for (int j = 0; j < npend; ++j) {
-    const SegDesc d = sm.done[sm.pend[j]];
-    if (!merge_request<D, G>(p, d, stages, p.stages * p.stage_bytes, &sm.ring_free,
-                             &sm.merge_full, hl, hg, HB, q_row_elems, n_free, n_full)) {
-      if (lane == 0) record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
-      return;
-    }
-  }
+  const float inv = 1.f / L;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(c.a.out) + (long long)t * Hq * D;
+  reinterpret_cast<uint2*>(out)[o_off] = packed;
 }
 
 // ------------------------------------------------------------------ host
@@ -822,7 +761,7 @@ cudaError_t launch_dg(const DecodeArgs& p, const CUtensorMap& mk, const CUtensor
     attr_set = true;
   }
   (void)num_requests;
-  return launch_pdl(kDecodeSplit, kern, dim3(p.num_ctas, hg), dim3(p.heads_per_cta * 32 + 64),
+  return launch_pdl(kDecodeSplit, kern, dim3(p.num_ctas, hg), dim3(p.heads_per_cta * 32 + 32),
                     smem, s, mk, mv, p);
 }
 
@@ -838,7 +777,31 @@ cudaError_t launch_d(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorM
   return cudaErrorInvalidValue;
 }
 
+template <int D>
+cudaError_t launch_combine_d(const CombineArgs& c, dim3 grid, dim3 block, cudaStream_t s) {
+  switch (c.a.num_q_heads / c.a.num_kv_heads) {
+    case 1: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 1>, grid, block, 0, s, c);
+    case 2: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 2>, grid, block, 0, s, c);
+    case 4: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 4>, grid, block, 0, s, c);
+    case 8: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 8>, grid, block, 0, s, c);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+cudaError_t launch_decode_combine(const CombineArgs& c, cudaStream_t stream) {
+  const int nx = c.n_entries >= 0 ? c.n_entries : c.a.num_requests;
+  if (nx <= 0) return cudaSuccess;
+  const int G = c.a.num_q_heads / c.a.num_kv_heads;
+  const int f4 = c.kv_per_cta * G * c.a.head_dim / 4;
+  if (c.kv_per_cta <= 0 || c.a.num_kv_heads % c.kv_per_cta != 0 || f4 > kCombineMaxThreads)
+    return cudaErrorInvalidValue;
+  const dim3 grid(nx, c.a.num_kv_heads / c.kv_per_cta);
+  const dim3 block((f4 + 31) / 32 * 32);
+  if (c.a.head_dim == 64) return launch_combine_d<64>(c, grid, block, stream);
+  return launch_combine_d<128>(c, grid, block, stream);
+}
 
 size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes) {
   return 1024 /* alignment slack */ + (size_t)stages * stage_bytes + 2 * (size_t)q_slot_bytes +

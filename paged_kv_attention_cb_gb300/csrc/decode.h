@@ -38,7 +38,6 @@ struct DecodeArgs {
                           // (graph replays: nothing in the arguments depends on the batch)
   float* part_o;          // [slots][Hq][D] unnormalised partial outputs
   float2* part_ml;        // [slots][Hq] (running max in log2 units, sum)
-  int* counters;          // [R][head groups] arrivals of split requests (zero between steps)
   int has_table;          // cta_first is filled (num_ctas <= kDecodeTableCtas)
   DecodeCtaStart cta_first[kDecodeTableCtas];
 };
@@ -47,8 +46,33 @@ struct DecodePlan {
   size_t smem_bytes;
 };
 
+// A request whose key blocks span several decode CTAs (b_first .. b_first + nseg - 1):
+// its partials sit in slots r + b_first .. r + b_first + nseg - 1.
+struct CombineEntry {
+  int r;
+  int t;        // its packed query row
+  int b_first;
+  int nseg;
+};
+
+constexpr int kCombineListMax = 256;    // split requests the host lists in the arguments
+constexpr int kCombineMaxThreads = 512;  // one per four outputs of a CTA's KV heads
+
+struct CombineArgs {
+  StepArgs a;
+  int num_ctas;           // C of the decode launch (its partition: CTA b takes [b U/C, (b+1) U/C))
+  const float* part_o;    // the decode launch's partials
+  const float2* part_ml;
+  int kv_per_cta;         // KV heads merged by one CTA (divides num_kv_heads; x G x D / 4 <= 512)
+  int n_entries;  // >= 0: entries[0 .. n_entries) are the split requests; -1: the
+                  // kernel finds them from the device metadata (one CTA per request)
+  CombineEntry entries[kCombineListMax];
+};
+
 size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes);
 cudaError_t launch_decode(DecodeArgs p, const DecodePlan& plan, cudaStream_t stream);
+// The merge of the split requests' partials, on the stream right after launch_decode.
+cudaError_t launch_decode_combine(const CombineArgs& c, cudaStream_t stream);
 // Kernel attributes the launch needs, set without launching (before a stream capture).
 cudaError_t prepare_decode(const DecodeArgs& p);
 

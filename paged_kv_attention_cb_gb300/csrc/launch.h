@@ -34,7 +34,8 @@ enum KernelId {
   kDecodeSplit = 2,
   kPrefillTc = 3,
   kCopyBlocks = 4,
-  kNumKernels = 5
+  kDecodeCombine = 5,
+  kNumKernels = 6
 };
 
 void note_launch_begin(KernelId id, cudaStream_t stream);

@@ -3,8 +3,8 @@
 // instance a plugin running inside a host program that owns the device memory
 // pool and forbids allocations on its inference path, or a latency-critical
 // caller that cannot afford the implicit device synchronisation of
-// cudaMalloc/cudaFree. The scratch the step needs (device error word,
-// split-request arrival counters, split-KV partial results) lives in a
+// cudaMalloc/cudaFree. The scratch the step needs (device error word and
+// split-KV partial results) lives in a
 // fixed-size device array compiled into this library instead of a
 // caller-provided workspace; the caller still passes every input and output.
 #include <cuda_runtime.h>
@@ -93,7 +93,7 @@ extern "C" cb_status cb_paged_attention_no_alloc(
                             "array (CB_NO_ALLOC_SCRATCH_BYTES); use cb_paged_attention with a "
                             "workspace");
 
-  // error word and arrival counters start at zero on every call
+  // the error word starts at zero on every call
   e = cudaMemsetAsync(scratch, 0, zeroed, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cb::report_cuda_error(e, "no-alloc scratch clear");
   return cb_paged_attention(out, q, k_cache, v_cache, k_new, v_new, slot_mapping, query_start_loc,

@@ -34,30 +34,26 @@ int sm_count() {
 }
 
 struct WorkspaceLayout {
-  size_t counters, part_ml, part_o, total;
+  size_t part_ml, part_o, total;
 };
 
 WorkspaceLayout layout(int32_t R, int32_t Hq, int32_t Hkv, int32_t D) {
+  (void)Hkv;
   WorkspaceLayout w;
   const size_t slots = (size_t)std::max(R, 0) + kMaxDecodeCtas;
-  const size_t head_groups = (size_t)(std::max(Hkv, 1) + kDecodeMaxHeads - 1) / kDecodeMaxHeads;
-  w.counters = kWorkspaceHeaderBytes;
-  w.part_ml = w.counters + align256((size_t)std::max(R, 1) * head_groups * 4);
+  w.part_ml = kWorkspaceHeaderBytes;
   w.part_o = w.part_ml + align256(slots * Hq * 8);
   w.total = w.part_o + slots * Hq * (size_t)D * 4;
   return w;
 }
 
 // The layout of a workspace of `bytes`: that of the largest request count it holds,
-// not of the step's own count, so that every step on one workspace finds the arrival
-// counters, the partial (m, l) and the partial outputs at the same offsets. (The
-// counters must read zero at the start of a step; with offsets that moved with the
-// request count, a larger step's counters could land where a smaller step left
-// partials.) The estimate is conservative: layout(R).total <= bytes.
+// not of the step's own count, so that every step on one workspace finds the
+// partial (m, l) and the partial outputs at the same offsets. The estimate is
+// conservative: layout(R).total <= bytes.
 WorkspaceLayout layout_of(size_t bytes, const StepArgs& a) {
   const size_t Hq = (size_t)a.num_q_heads, D = (size_t)a.head_dim;
-  const size_t hg = (size_t)(std::max(a.num_kv_heads, 1) + kDecodeMaxHeads - 1) / kDecodeMaxHeads;
-  const size_t per_request = hg * 4 + Hq * 8 + Hq * D * 4;
+  const size_t per_request = Hq * 8 + Hq * D * 4;
   const size_t fixed = kWorkspaceHeaderBytes + 512 + (size_t)kMaxDecodeCtas * (Hq * 8 + Hq * D * 4);
   long long r = bytes > fixed ? (long long)((bytes - fixed) / per_request) : 0;
   r = std::min<long long>(r, 1 << 24);
@@ -69,6 +65,29 @@ WorkspaceLayout layout_of(size_t bytes, const StepArgs& a) {
 int kb_lo_host(int seq, int window) { return (window > 0 ? std::max(0, seq - window) : 0) / 16; }
 
 int decode_units_host(int seq, int window) { return (seq - 1) / 16 - kb_lo_host(seq, window) + 1; }
+
+// CTA of the decode partition that owns global key block u (ranges [b U/C, (b+1) U/C)).
+int cta_of_host(long long u, long long U, int C) { return (int)(((u + 1) * C + U - 1) / U) - 1; }
+
+void combine_common(CombineArgs& c, const StepArgs& a, const DecodeArgs& d) {
+  c.a = a;
+  c.num_ctas = d.num_ctas;
+  c.part_o = d.part_o;
+  c.part_ml = d.part_ml;
+}
+
+// KV heads per combine CTA for `n` requests to merge: the fewest (most CTAs) that
+// keep the grid within about one CTA per SM, a divisor of Hkv, and at most
+// kCombineMaxThreads threads (four outputs each) per CTA.
+int combine_kv_per_cta(const StepArgs& a, int n) {
+  const int Hkv = a.num_kv_heads, G = a.num_q_heads / a.num_kv_heads;
+  int best = 0;
+  for (int k = Hkv; k >= 1; --k) {
+    if (Hkv % k != 0 || k * G * a.head_dim / 4 > kCombineMaxThreads) continue;
+    if (best == 0 || (long long)std::max(n, 1) * (Hkv / k) <= sm_count()) best = k;
+  }
+  return best;
+}
 
 }  // namespace
 
@@ -87,6 +106,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   plan.fast_prefill = false;
   plan.n_prefill_launches = 0;
   plan.portable_mode = 0;
+  plan.has_combine = false;
   if ((flags & CB_FLAG_PORTABLE_ONLY) || a.dtype == CB_F32) return;
 
   // ---- which rows exist
@@ -139,11 +159,31 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     }
     const WorkspaceLayout w = layout_of(workspace_bytes, a);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    d.counters = reinterpret_cast<int*>(ws + w.counters);
     d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     d.part_o = reinterpret_cast<float*>(ws + w.part_o);
     plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
     if (d.stages >= 2) plan.fast_decode = true;
+    // the requests split over several CTAs, merged by the combine launch
+    CombineArgs& c = plan.combine;
+    combine_common(c, a, d);
+    c.n_entries = 0;
+    long long u = 0;
+    for (int r = 0; r < a.num_requests; ++r) {
+      const int ql = h_qsl[r + 1] - h_qsl[r];
+      if (ql != 1 || h_seq_lens[r] <= 0) continue;
+      const int units = decode_units_host(h_seq_lens[r], a.sliding_window);
+      const int b0 = cta_of_host(u, U, d.num_ctas);
+      const int b1 = cta_of_host(u + units - 1, U, d.num_ctas);
+      u += units;
+      if (b1 == b0) continue;
+      if (c.n_entries == kCombineListMax) {
+        c.n_entries = -1;  // too many to list: the kernel finds them
+        break;
+      }
+      c.entries[c.n_entries++] = CombineEntry{r, h_qsl[r], b0, b1 - b0 + 1};
+    }
+    c.kv_per_cta = combine_kv_per_cta(a, c.n_entries >= 0 ? c.n_entries : a.num_requests);
+    plan.has_combine = plan.fast_decode && c.n_entries != 0;
   }
 
   // ---- prefill rows: tcgen05 tile kernel, heaviest requests first
@@ -201,6 +241,7 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   plan.fast_prefill = false;
   plan.n_prefill_launches = 0;
   plan.portable_mode = -1;
+  plan.has_combine = false;
   if (a.dtype != CB_BF16) return false;
   const int G = a.num_q_heads / a.num_kv_heads;
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
@@ -223,12 +264,15 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   d.has_table = 0;
   const WorkspaceLayout w = layout_of(workspace_bytes, a);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  d.counters = reinterpret_cast<int*>(ws + w.counters);
   d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
   d.part_o = reinterpret_cast<float*>(ws + w.part_o);
   plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
   if (d.stages < 2) return false;
   plan.fast_decode = with_decode;
+  combine_common(plan.combine, a, d);
+  plan.combine.n_entries = -1;  // the batch's split requests are found on the device
+  plan.combine.kv_per_cta = combine_kv_per_cta(a, a.num_requests);
+  plan.has_combine = with_decode;
 
   PrefillArgs& pa = plan.prefill[0];
   pa.a = a;
@@ -259,12 +303,15 @@ size_t workspace_extent(const Plan& plan, const StepArgs& a) {
 }
 
 size_t workspace_zeroed_prefix(const StepArgs& a, size_t workspace_bytes) {
-  return layout_of(workspace_bytes, a).part_ml;
+  (void)a;
+  (void)workspace_bytes;
+  return kWorkspaceHeaderBytes;  // the error word
 }
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {
   if (plan.fast_decode) {
     cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);
+    if (e == cudaSuccess && plan.has_combine) e = launch_decode_combine(plan.combine, stream);
     if (e != cudaSuccess) return e;
   }
   for (int l = 0; l < plan.n_prefill_launches && plan.fast_prefill; ++l) {

@@ -26,6 +26,8 @@ struct Plan {
   size_t workspace_bytes;
   DecodeArgs decode;
   DecodePlan decode_plan;
+  bool has_combine;     // a combine launch follows the decode launch
+  CombineArgs combine;
   int n_prefill_launches;
   PrefillArgs prefill[kMaxPrefillLaunches];
 };
@@ -49,7 +51,7 @@ cudaError_t prepare_plan(const Plan& plan, const StepArgs& a);
 
 // Bytes at the start of the workspace that the planned launch reads or writes
 // (the rest of a cb_workspace_size() buffer is headroom for larger plans), and
-// the leading part of it that must be zero before a call (error word, counters).
+// the leading part of it that must be zero before a call (the error word).
 // The workspace's layout depends on its size only, never on the step's request
 // count, so that steps of any size can share one workspace.
 size_t workspace_extent(const Plan& plan, const StepArgs& a);

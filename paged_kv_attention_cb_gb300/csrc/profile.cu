@@ -40,7 +40,7 @@ cudaEvent_t take_event() {
 }
 
 const char* const kNames[kNumKernels] = {"write_kv", "portable_attention", "decode_split",
-                                         "prefill_tc", "copy_blocks"};
+                                         "prefill_tc", "copy_blocks", "decode_combine"};
 
 }  // namespace
 

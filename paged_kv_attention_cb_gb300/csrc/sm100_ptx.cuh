@@ -95,6 +95,31 @@ CB_DEV void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       : "memory");
 }
 
+// An L2 cache policy that marks the lines an access brings in as the first to
+// evict: for data read once (the decode KV stream), so that it does not push out
+// of L2 what is read again soon (the split partials).
+CB_DEV uint64_t l2_policy_evict_first() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+// tma_load_4d with an L2 cache policy for the lines it reads.
+CB_DEV void tma_load_4d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                             int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// Hint that the line holding `p` be brought into L2 (no effect on the values read).
+CB_DEV void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
 CB_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
