@@ -156,6 +156,12 @@ cb_status cb_workspace_init(void* workspace, size_t workspace_bytes, void* strea
  * If k_new is not NULL the step first scatters k_new/v_new through
  * slot_mapping exactly as cb_write_kv does, then attends: the attended range
  * reaches this step's own tokens, which are read back from the cache.
+ * slot_mapping must send each row to the slot of its own position (or < 0,
+ * or to pages no request of the step reads, such as the reserved padding
+ * pages), as a scheduler builds it: a step made of decode rows only (every
+ * q_len <= 1) is run without a separate scatter launch -- the decode kernel
+ * writes each row where it reads that position, so a slot pointing into a
+ * position another request reads in the same step would race.
  * For every request r, row t = query_start_loc[r] + i (0 <= i < q_len) and
  * query head h, with g = h / (Hq / Hkv) and positions
  * p in [lo, context_len + i], lo = 0 or, with sliding_window W > 0,

@@ -239,6 +239,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // the KV stream is read once: it leaves L2 first, ahead of the partials that
     // the combine kernel reads back
     const uint64_t kv_policy = l2_policy_evict_first();
+
     bool ok = true;
     int wbase = -1, w_units = 0, w_seq = 0, w_t = 0;
     auto load_window = [&](int r0) {
@@ -422,6 +423,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   // ===================================================== consumer warps
   const int hl = warp;  // local KV head
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's K (or V) row
+  const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
   const int gid = lane >> 2;
   const int tq = lane & 3;
   const float sl2 = p.a.scale_log2;
@@ -434,6 +437,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const SegDesc d = sm.seg[qs];
     if (d.r < 0) break;
+    // fused scatter (steps of decode rows only): the segment holding the request's
+    // last key block takes the request's new K/V row of this warp's head -- lane c <
+    // kRowChunks: 16-byte chunk c of K, the next kRowChunks lanes the same chunks of V --
+    // writes it to the row's cache slot and over the stale copy of that position in the
+    // staged block, so no other CTA and no copy engine needs to see the write
+    const int kb_last = d.hi / kKB;
+    const bool fused_row = p.fuse_scatter && d.kb1 == kb_last + 1;
+    long long row_slot = -1;
+    uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+    if (fused_row) {
+      row_slot = __ldg(p.slot_mapping + d.t);
+      if (lane < 2 * kRowChunks) {
+        const uint4* src = static_cast<const uint4*>(lane < kRowChunks ? p.k_new : p.v_new);
+        new_row = __ldg(src + ((long long)d.t * p.a.num_kv_heads + hg * HB + hl) * kRowChunks +
+                        lane % kRowChunks);
+      }
+    }
     // query fragments (B operand of S^T = K Q^T): Q[head = gid][d = 16ks + 2tq (+8)]
     uint32_t qf[kKSteps][2];
     {
@@ -459,9 +479,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
         return;
       }
-      const uint8_t* ks_base = stages + s * p.stage_bytes;
+      uint8_t* ks_base = stages + s * p.stage_bytes;
       uint8_t* vs_base = stages + s * p.stage_bytes + kHalves * box_bytes;
       const int key_base = kb * kKB;
+      if (fused_row && kb == kb_last) {
+        if (row_slot >= 0 && row_slot < num_slots) {
+          if (lane < 2 * kRowChunks) {
+            const int c = lane % kRowChunks;
+            const int key = d.hi - key_base;
+            uint8_t* tile = lane < kRowChunks ? ks_base : vs_base;
+            *reinterpret_cast<uint4*>(tile + (c >> 3) * box_bytes + (hl * kKB + key) * 128 +
+                                      (((c & 7) ^ (key & 7)) << 4)) = new_row;
+            uint4* cache = static_cast<uint4*>(lane < kRowChunks ? p.a.k_cache : p.a.v_cache);
+            cache[(row_slot * p.a.num_kv_heads + hg * HB + hl) * kRowChunks + c] = new_row;
+          }
+        } else if (row_slot >= num_slots && lane == 0) {
+          record_error(p.a.error_word, CB_DEVERR_SLOT_CODE);
+        }
+        __syncwarp();
+      }
       // zero V rows past the last attended key (their page slots hold unrelated data)
       if (key_base + kKB - 1 > d.hi) {
         const int first_bad = d.hi - key_base + 1;

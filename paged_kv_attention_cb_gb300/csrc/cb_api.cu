@@ -299,10 +299,11 @@ cb_status paged_attention_impl(cb_graph_cache* graph, void* out, const void* q, 
 
   cb::Plan plan;
   if (!graph) {
-    cudaError_t e = scatter();
+    const cb::ScatterInputs rows{k_new, v_new, slot_mapping};
+    cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new ? &rows : nullptr,
+                  workspace, workspace_bytes);
+    cudaError_t e = plan.fused_scatter ? cudaSuccess : scatter();
     if (e != cudaSuccess) return cuda_fail(e, "write_kv launch");
-    cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, workspace,
-                  workspace_bytes);
     e = cb::run_plan(plan, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return CB_OK;

@@ -12,6 +12,7 @@ constexpr int kDecodeMaxHeads = 8;          // KV heads per CTA (one consumer wa
 constexpr int kDecodeSmemLimit = 232448;    // 227 KiB dynamic shared memory per CTA
 constexpr int kDecodeTableCtas = 256;       // CTAs whose start is passed in the arguments
 constexpr int CB_DEVERR_BLOCK_ID_CODE = 0x1;
+constexpr int CB_DEVERR_SLOT_CODE = 0x2;
 constexpr int CB_DEVERR_TIMEOUT_CODE = 0x4;
 
 // Where CTA b's range of key blocks starts, placed by the host from its mirrors of
@@ -38,6 +39,15 @@ struct DecodeArgs {
                           // (graph replays: nothing in the arguments depends on the batch)
   float* part_o;          // [slots][Hq][D] unnormalised partial outputs
   float2* part_ml;        // [slots][Hq] (running max in log2 units, sum)
+  // Steps of decode rows only: the CTA that reads a request's last key block writes
+  // the request's new K/V row (its heads) into the row's slot and into its staged
+  // copy of that block, so the step needs no separate scatter launch. The row's slot
+  // must be that of the request's last position (or < 0: not written), as a
+  // scheduler-built slot_mapping has it.
+  int fuse_scatter;
+  const void* k_new;      // [T, Hkv, D]
+  const void* v_new;
+  const int64_t* slot_mapping;
   int has_table;          // cta_first is filled (num_ctas <= kDecodeTableCtas)
   DecodeCtaStart cta_first[kDecodeTableCtas];
 };

@@ -83,7 +83,9 @@ extern "C" cb_status cb_paged_attention_no_alloc(
   size_t zeroed = cb::kWorkspaceHeaderBytes;
   if (plannable) {
     cb::Plan plan;
-    cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new != nullptr, scratch, bound);
+    const cb::ScatterInputs rows{k_new, v_new, slot_mapping};
+    cb::plan_step(plan, a, h_query_start_loc, h_seq_lens, flags, k_new ? &rows : nullptr, scratch,
+                  bound);
     extent = cb::workspace_extent(plan, a);
     zeroed = cb::workspace_zeroed_prefix(a, bound);
   }

@@ -99,7 +99,9 @@ size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_h
 }
 
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
-               uint32_t flags, bool scatter_first, void* workspace, size_t workspace_bytes) {
+               uint32_t flags, const ScatterInputs* scatter, void* workspace,
+               size_t workspace_bytes) {
+  bool scatter_first = scatter != nullptr;
   plan.workspace = workspace;
   plan.workspace_bytes = workspace_bytes;
   plan.fast_decode = false;
@@ -107,6 +109,7 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   plan.n_prefill_launches = 0;
   plan.portable_mode = 0;
   plan.has_combine = false;
+  plan.fused_scatter = false;
   if ((flags & CB_FLAG_PORTABLE_ONLY) || a.dtype == CB_F32) return;
 
   // ---- which rows exist
@@ -133,8 +136,14 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     d.q_slot_bytes = HB * G * a.head_dim * 2;
     const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
     d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
-    d.metadata_ready = scatter_first ? 1 : 0;
     d.units_on_device = 0;
+    // a step of decode rows only: each row's new K/V is written by the CTA that
+    // reads the request's last key block (the decode kernel is the step's first)
+    d.fuse_scatter = scatter != nullptr && !has_prefill ? 1 : 0;
+    d.k_new = scatter ? scatter->k_new : nullptr;
+    d.v_new = scatter ? scatter->v_new : nullptr;
+    d.slot_mapping = scatter ? scatter->slot_mapping : nullptr;
+    d.metadata_ready = scatter_first && !d.fuse_scatter ? 1 : 0;
     // where each CTA's range [b*U/C, (b+1)*U/C) starts: (request, its first unit)
     d.has_table = d.num_ctas <= kDecodeTableCtas;
     if (d.has_table) {
@@ -163,6 +172,9 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     d.part_o = reinterpret_cast<float*>(ws + w.part_o);
     plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
     if (d.stages >= 2) plan.fast_decode = true;
+    if (!plan.fast_decode) d.fuse_scatter = 0;
+    plan.fused_scatter = d.fuse_scatter != 0;
+    if (plan.fused_scatter) scatter_first = false;
     // the requests split over several CTAs, merged by the combine launch
     CombineArgs& c = plan.combine;
     combine_common(c, a, d);
@@ -242,6 +254,7 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   plan.n_prefill_launches = 0;
   plan.portable_mode = -1;
   plan.has_combine = false;
+  plan.fused_scatter = false;
   if (a.dtype != CB_BF16) return false;
   const int G = a.num_q_heads / a.num_kv_heads;
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
@@ -261,6 +274,9 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
   d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
   d.metadata_ready = 0;
+  d.fuse_scatter = 0;
+  d.k_new = d.v_new = nullptr;
+  d.slot_mapping = nullptr;
   d.has_table = 0;
   const WorkspaceLayout w = layout_of(workspace_bytes, a);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -18,10 +18,18 @@ constexpr int kMaxPrefillLaunches = 8;         // x kPrefillMaxEntries prefill r
 size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim);
 
+// The step's new K/V rows: cb_paged_attention's k_new / v_new / slot_mapping.
+struct ScatterInputs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+};
+
 struct Plan {
   int portable_mode;   // -1: none, 0: all rows, 1: decode rows, 2: prefill rows
   bool fast_decode;    // decode rows on the split-KV tensor-core kernel
   bool fast_prefill;   // prefill rows on the tcgen05 tile kernel
+  bool fused_scatter;  // the decode kernel writes the new K/V rows (no scatter launch)
   void* workspace;
   size_t workspace_bytes;
   DecodeArgs decode;
@@ -32,8 +40,11 @@ struct Plan {
   PrefillArgs prefill[kMaxPrefillLaunches];
 };
 
+// scatter: the step's new rows (nullptr: none). Unless the plan fuses them into the
+// decode kernel (fused_scatter), the caller launches the scatter before run_plan.
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
-               uint32_t flags, bool scatter_first, void* workspace, size_t workspace_bytes);
+               uint32_t flags, const ScatterInputs* scatter, void* workspace,
+               size_t workspace_bytes);
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream);
 

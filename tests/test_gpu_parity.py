@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_cb_gb300 as cb
 import workloads
 from stepcheck import (GpuStep, cache_bits, compare, oracle_cache_bits, oracle_step, sample_rows)
@@ -17,19 +18,26 @@ pytestmark = pytest.mark.gpu
 PATHS = {"fast": 0, "portable": cb.CB_FLAG_PORTABLE_ONLY}
 
 
+def check_scatter(st, k_before, v_before):
+    """K and V caches after the step: bit-exact against the oracle's scatter, outside the
+    reserved pages 0-1 (where padding rows may land)."""
+    spec = st.spec
+    for name, before in (("k", k_before), ("v", v_before)):
+        want = oracle_cache_bits(spec, before, st.x[name + "_new"], spec.slot_mapping)
+        got = cache_bits(st.x[name + "_cache"])
+        assert np.array_equal(got[2:], want[2:]), name
+
+
 def full_check(spec, flags=0, scale=None, max_abs=None, mean_abs=None):
     st = GpuStep(spec)
     h = st.host_inputs()
-    k_before = st.x["k_cache"].clone()
+    k_before, v_before = st.x["k_cache"].clone(), st.x["v_cache"].clone()
     out = st.run(flags=flags, scale=scale)
     torch.cuda.synchronize()
     assert cb.read_error_word(st.ws) == 0
     ref = oracle_step(spec, h, scale=scale)
     mx, mn = compare(spec, out, ref, max_abs=max_abs, mean_abs=mean_abs)
-    # scatter bit-exact outside the reserved pages
-    want = oracle_cache_bits(spec, k_before, st.x["k_new"], spec.slot_mapping)
-    got = cache_bits(st.x["k_cache"])
-    assert np.array_equal(got[2:], want[2:])
+    check_scatter(st, k_before, v_before)
     return mx, mn
 
 
@@ -90,11 +98,13 @@ def test_sharp_softmax():
 def sampled_check(spec, n_rows=64, flags=0):
     st = GpuStep(spec)
     h = st.host_inputs()
+    k_before, v_before = st.x["k_cache"].clone(), st.x["v_cache"].clone()
     out = st.run(flags=flags)
     torch.cuda.synchronize()
     assert cb.read_error_word(st.ws) == 0
     rows = sample_rows(spec, n_rows)
     ref = oracle_step(spec, h, rows=rows)
+    check_scatter(st, k_before, v_before)
     return compare(spec, out, ref, rows=rows)
 
 
@@ -188,6 +198,34 @@ def test_out_of_range_slot_is_recorded_and_skipped():
     torch.cuda.synchronize()
     assert torch.equal(before, st.x["k_cache"])
     assert cb.read_error_word(st.ws) & 0x2
+
+
+def test_decode_step_scatter_skips_negative_and_records_out_of_range_slots():
+    """A step of decode rows only writes its rows from the decode kernel itself: a slot
+    below zero is skipped, one past the pool is recorded (0x2) and skipped, the rest land
+    bit-exactly and the rows whose slot was written attend to their new K/V."""
+    spec = workloads.custom([1] * 5, [40, 700, 3, 1500, 90], num_q_heads=16, num_kv_heads=4,
+                            seed=21)
+    st = GpuStep(spec)
+    slots = spec.slot_mapping.copy()
+    slots[1] = -1
+    slots[3] = spec.num_blocks * spec.block_size + 5
+    st.md["slot_mapping"] = torch.from_numpy(slots).cuda()
+    h = st.host_inputs()
+    k_before, v_before = st.x["k_cache"].clone(), st.x["v_cache"].clone()
+    out = st.run()
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) & 0x2
+    kept = slots.copy()
+    kept[3] = -1  # what the kernel did with the slot past the pool: nothing
+    for name, before in (("k", k_before), ("v", v_before)):
+        want = oracle_cache_bits(spec, before, st.x[name + "_new"], kept)
+        assert np.array_equal(cache_bits(st.x[name + "_cache"])[2:], want[2:]), name
+    # rows 0, 2, 4 attend to their new K/V; rows 1 and 3 to what the cache held
+    oracle.scatter_kv(h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], kept)
+    ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], spec.query_start_loc,
+                                 spec.seq_lens, spec.block_table, spec.block_size, spec.scale)
+    compare(spec, out, ref)
 
 
 # ------------------------------------------------------------------ decode kernel coverage
