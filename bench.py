@@ -41,6 +41,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import hashlib
+import datetime
 import json
 import statistics
 import subprocess
@@ -118,29 +119,56 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons around a timed region.
+
+    Sampling starts before the region (the `with` block) and runs until a sample after
+    it has arrived; the summary takes the samples stamped inside the region, or, for a
+    region shorter than the sampling period, the two samples that bracket it."""
+
+    PERIOD_MS = 50
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
         # raw samples (the JSON line carries their summary); CB_BENCH_CLOCKS_DIR keeps them
         self.path = os.path.join(os.environ.get("CB_BENCH_CLOCKS_DIR", tempfile.gettempdir()),
                                  f"bench_clocks_{os.getpid()}.csv")
 
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return f.read().splitlines()
+        except OSError:
+            return []
+
+    def _wait_for(self, pred, timeout_s):
+        end = time.time() + timeout_s
+        while time.time() < end:
+            if pred(self._rows()):
+                return
+            time.sleep(0.01)
+
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            self.f = open(self.path, "w", buffering=1)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=self.f, stderr=subprocess.DEVNULL)
+            self._wait_for(lambda rows: len(rows) >= 1, 5.0)  # sampling is live
         except Exception:
             self.proc = None
+        self.t0 = datetime.datetime.now()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = datetime.datetime.now()
         if self.proc is not None:
+            self._wait_for(lambda rows: any(r[0] > self.t1 for r in rows), 2.0)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -148,30 +176,42 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
+    def _rows(self):
+        rows = []
+        for line in self._lines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(parts[2].split()[0]), float(parts[3].split()[0]),
+                             parts[6:10]))
+            except ValueError:
+                continue
+        return rows
+
     def summary(self):
-        if self.proc is None:
+        if self.proc is None or self.t0 is None or self.t1 is None:
             return None
-        sm, mx, reasons = [], [], set()
+        rows = self._rows()
+        inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+        window = "inside"
+        if not inside:
+            before = [r for r in rows if r[0] < self.t0][-1:]
+            after = [r for r in rows if r[0] > self.t1][:1]
+            inside = before + after
+            window = "bracketing (timed region shorter than the sampling period)"
+        if not inside:
+            return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        try:
-            for line in open(self.path):
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1].split()[0]))
-                    mx.append(float(parts[2].split()[0]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        except OSError:
-            return None
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "window": window, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- distributed
@@ -853,7 +893,9 @@ def copy_main(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 1000 for the GPU arm, so that the timed "
+                         "region spans several clock samples; 10 for the oracle arm)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode",
@@ -869,6 +911,8 @@ def main():
     ap.add_argument("--flush", choices=["read", "write"], default="read",
                     help="L2 eviction between timed steps: read (clean) or write (dirty) 512 MiB")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 1000 if args.impl == "ours" else 10
     if args.warmup < 3:
         args.warmup = 3
 
