@@ -59,6 +59,11 @@ import workloads  # noqa: E402
 FLUSH_BYTES = 512 << 20
 GRAPH_Q_INTERVAL = 64  # query padding interval of --graph (the decode step's 64 requests fit)
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# the default line: the long-context decode step (the largest single-GPU workload), with the
+# mixed continuous-batching step and the windowed long decode measured beside it
+DEFAULT_CONFIG = "long_decode"
+EXTRA_CONFIGS = ("mixed", "long_decode_window")
 
 
 # ---------------------------------------------------------------- accounting
@@ -83,6 +88,22 @@ def decode_kernel_bytes(spec) -> int:
     return n
 
 
+def prefill_flops(spec) -> int:
+    """Algorithmic FLOPs of the prefill rows (q_len > 1): 4 x Hq x D per attended
+    (query, key) pair -- the causal (and windowed) pairs only, not the dense tiles."""
+    pairs = 0
+    for r in range(spec.R):
+        ql = int(spec.q_lens[r])
+        if ql <= 1:
+            continue
+        ctx = int(spec.ctx_lens[r])
+        for i in range(ql):
+            hi = ctx + i
+            lo = 0 if spec.sliding_window <= 0 else max(0, hi - spec.sliding_window + 1)
+            pairs += hi - lo + 1
+    return 4 * spec.num_q_heads * spec.head_dim * pairs
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -91,6 +112,16 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 TFLOP/s for a kernel timed alone (burst), and where it comes from."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_sha(name: str) -> str:
@@ -348,28 +379,34 @@ def run_ours(args, spec, world, rank, local):
     per_kernel = cb.kernel_timing_collect()
     cb.kernel_timing(False)
 
-    # ---- end to end through the public API: pinned host inputs in, result out
-    host_in = {k: v.cpu().pin_memory() for k, v in (("q", x["q"]), ("k_new", x["k_new"]),
-                                                     ("v_new", x["v_new"]))}
-    host_md = {k: v.cpu().pin_memory() for k, v in md.items()}
+    # ---- end to end through the public API: pinned host inputs in, result out. The
+    # step's inputs (q, k_new, v_new and the four metadata arrays) sit packed in one pinned
+    # host buffer and go over in one copy; the output comes back in one copy.
+    parts = [("q", x["q"]), ("k_new", x["k_new"]), ("v_new", x["v_new"])] + list(md.items())
+    offs, total = {}, 0
+    for k, v in parts:
+        offs[k] = total
+        total += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, k, like):
+        n = like.numel() * like.element_size()
+        return buf[offs[k]:offs[k] + n].view(like.dtype).view(like.shape)
+
+    for k, v in parts:
+        view(host_buf, k, v).copy_(v.cpu())
+    dv = {k: view(dev_buf, k, v) for k, v in parts}
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    dev_md = {k: torch.empty_like(v, device=dev) for k, v in host_md.items()}
-    h2d = sum(v.numel() * v.element_size() for v in list(host_in.values()) + list(host_md.values()))
+    h2d = sum(v.numel() * v.element_size() for _, v in parts)
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for k in dev_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        for k in dev_md:
-            dev_md[k].copy_(host_md[k], non_blocking=True)
-        attention(out, dev_in["q"], x["k_cache"], x["v_cache"],
-                           dev_md["query_start_loc"], dev_md["seq_lens"], dev_md["block_table"],
-                           spec.query_start_loc, spec.seq_lens, ws, scale=spec.scale,
-                           sliding_window=spec.sliding_window,
-                           k_new=dev_in["k_new"],
-                           v_new=dev_in["v_new"], slot_mapping=dev_md["slot_mapping"],
-                           stream=stream)
+        dev_buf.copy_(host_buf, non_blocking=True)
+        attention(out, dv["q"], x["k_cache"], x["v_cache"], dv["query_start_loc"],
+                  dv["seq_lens"], dv["block_table"], spec.query_start_loc, spec.seq_lens, ws,
+                  scale=spec.scale, sliding_window=spec.sliding_window, k_new=dv["k_new"],
+                  v_new=dv["v_new"], slot_mapping=dv["slot_mapping"], stream=stream)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -447,6 +484,7 @@ def run_ours(args, spec, world, rank, local):
         g2.close()
     return dict(ms_per_step=ms_per_step, step_ms=step_ms, launches=launches, alt_ms=alt_ms,
                 per_kernel=per_kernel, e2e_ms_per_step=e2e_ms / args.steps, h2d=h2d, d2h=d2h,
+                h2d_copies=1,
                 clocks=clocks.summary(), graph=graph_info)
 
 
@@ -620,39 +658,49 @@ def run_trace_ours(args, cfg, specs, world, rank, local):
     per_kernel = cb.kernel_timing_collect()
     cb.kernel_timing(False)
 
-    # end to end: each step's inputs and metadata from pinned host memory, output back
-    hq = torch.empty(max_t * cfg.num_q_heads * cfg.head_dim, dtype=torch.bfloat16, pin_memory=True)
-    hk = torch.empty(max_t * cfg.num_kv_heads * cfg.head_dim, dtype=torch.bfloat16, pin_memory=True)
-    hv = torch.empty_like(hk, pin_memory=True)
-    ho = torch.empty_like(hq, pin_memory=True)
-    dq = torch.empty_like(out_buf)
-    dk = torch.empty(max_t, cfg.num_kv_heads, cfg.head_dim, dtype=torch.bfloat16, device=dev)
-    dvv = torch.empty_like(dk)
+    # end to end: each step's inputs and metadata packed in one pinned host buffer and
+    # copied in one transfer; the output back in one transfer
+    def packed(parts):
+        offs, total = {}, 0
+        for k, v in parts:
+            offs[k] = total
+            total += (v.numel() * v.element_size() + 255) // 256 * 256
+        return offs, total
+
+    sizes = [packed([("q", q), ("k", kn), ("v", vn)] + list(md.items()))[1]
+             for _, q, kn, vn, md in steps[:n]]
+    cap = max(sizes) if sizes else 256
+    host_buf = torch.empty(cap, dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ho = torch.empty(max_t * cfg.num_q_heads * cfg.head_dim, dtype=torch.bfloat16,
+                     pin_memory=True)
     e2e_ms = 0.0
     h2d = d2h = 0
     for i in range(n):
         sp, q, kn, vn, md = steps[i]
-        nq, nk = q.numel(), kn.numel()
-        hq[:nq].copy_(q.view(-1))
-        hk[:nk].copy_(kn.view(-1))
-        hv[:nk].copy_(vn.view(-1))
-        hmd = {k: v.cpu().pin_memory() for k, v in md.items()}
-        dmd = {k: torch.empty_like(v, device=dev) for k, v in hmd.items()}
+        parts = [("q", q), ("k", kn), ("v", vn)] + list(md.items())
+        offs, total = packed(parts)
+
+        def view(buf, k, like):
+            nb = like.numel() * like.element_size()
+            return buf[offs[k]:offs[k] + nb].view(like.dtype).view(like.shape)
+
+        for k, v in parts:
+            view(host_buf, k, v).copy_(v.cpu())
+        dvs = {k: view(dev_buf, k, v) for k, v in parts}
+        dmd = {k: dvs[k] for k in md}
+        nq = q.numel()
         torch.cuda.synchronize()
         flush_buf.max()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        dq[:sp.T].view(-1).copy_(hq[:nq], non_blocking=True)
-        dk[:sp.T].view(-1).copy_(hk[:nk], non_blocking=True)
-        dvv[:sp.T].view(-1).copy_(hv[:nk], non_blocking=True)
-        for k in dmd:
-            dmd[k].copy_(hmd[k], non_blocking=True)
-        call(i, dq[:sp.T], dk[:sp.T], dvv[:sp.T], dmd)
+        dev_buf[:total].copy_(host_buf[:total], non_blocking=True)
+        call(i, dvs["q"], dvs["k"], dvs["v"], dmd)
         ho[:nq].copy_(out_buf[:sp.T].view(-1), non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms += a.elapsed_time(b)
-        h2d += 2 * (nq + 2 * nk) + sum(v.numel() * v.element_size() for v in hmd.values())
+        h2d += sum(v.numel() * v.element_size() for _, v in parts)
         d2h += 2 * nq
     return dict(step_ms=step_ms, launches=launches, per_kernel=per_kernel, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, clocks=clocks.summary())
@@ -898,7 +946,7 @@ def main():
                          "region spans several clock samples; 10 for the oracle arm)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="decode",
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
                     choices=sorted(workloads.CONFIGS) + ["trace", "trace_prefill_first",
                                                          "copy_blocks"])
     ap.add_argument("--graph", action="store_true",
@@ -908,6 +956,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", dest="extras", action="store_true", default=None,
+                    help="also measure the mixed step and the windowed long decode and report "
+                         "them in the same line (default: on for the default workload)")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--flush", choices=["read", "write"], default="read",
                     help="L2 eviction between timed steps: read (clean) or write (dirty) 512 MiB")
     args = ap.parse_args()
@@ -915,6 +967,8 @@ def main():
         args.steps = 1000 if args.impl == "ours" else 10
     if args.warmup < 3:
         args.warmup = 3
+    if args.extras is None:
+        args.extras = args.config == DEFAULT_CONFIG and args.impl == "ours" and not args.graph
 
     world, rank, local = dist_setup()
     metric = "paged-attn step: achieved KV-read HBM GB/s & query tokens/s; % of roofline"
@@ -969,32 +1023,14 @@ def main():
         return
 
     res = run_ours(args, spec, world, rank, local)
+    extras = {}
+    if args.extras:
+        for name in EXTRA_CONFIGS:
+            xs = workloads.by_name(name)
+            extras[name] = (xs, run_ours(args, xs, world, rank, local))
     if rank != 0:
         return
-    ms = res["ms_per_step"]
-    value = world * kvb / (ms * 1e-3) / 1e9
-    tok_s = world * spec.T / (ms * 1e-3)
-    peak, peak_kind = peaks()
-
-    # dominant kernel: most device time in the attribution pass
-    pk = res["per_kernel"]
-    dom = max(pk.items(), key=lambda kv: kv[1][0])[0] if pk else None
-    dom_ms = pk[dom][0] / pk[dom][1] if dom else None
-    if dom == "decode_split":
-        dom_bytes, src = decode_kernel_bytes(spec), "attn_decode.cu"
-    elif dom == "portable_attention":
-        dom_bytes, src = kvb + 2 * spec.T * spec.num_q_heads * spec.head_dim * spec.elt_bytes(), \
-            "attn_portable.cu"
-    else:
-        dom_bytes, src = kvb, ""
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-                "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "algorithmic_bytes_per_launch": dom_bytes,
-                "avg_launch_ms": dom_ms,
-                "traffic": recorded_traffic(dom, spec.name) if dom else None}
-
+    line = workload_summary(spec, res, world)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         sample, what = oracle_sample_spec(spec, oracle_sample_size(args.config))
@@ -1002,25 +1038,79 @@ def main():
         cpu = {"value": kv_bytes(sample) * n / el / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{what} x {n} oracle steps in {el:.1f} s",
                "all_cores": oracle_all_cores(args.config, min(args.cpu_budget, 10.0))}
+    out = {"metric": metric, "value": line.pop("value"), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": line.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16" if spec.dtype == "bf16" else "f32", "data": "synthetic",
+           "config": cfg}
+    out.update(line)
+    out["cpu_baseline"] = cpu
+    if extras:
+        out["extra_workloads"] = {}
+        for name, (xs, xr) in extras.items():
+            xl = workload_summary(xs, xr, world)
+            xl["workload"] = xs.name
+            out["extra_workloads"][name] = xl
+            if name == "mixed" and xl.get("roofline_prefill"):
+                # the tensor-core roofline of the prefill tile kernel, on the mixed step
+                out["roofline_prefill"] = dict(xl["roofline_prefill"], workload=xs.name)
+    if res.get("graph"):
+        out["graph"] = res["graph"]
+    print(json.dumps(out), flush=True)
 
-    e2e_ms = res["e2e_ms_per_step"]
-    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-            if spec.dtype == "bf16" else "f32", "data": "synthetic", "config": cfg,
-            "tokens_per_s": tok_s,
+
+def workload_summary(spec, res, world):
+    """Throughput, end-to-end figure and rooflines of one workload's run_ours result."""
+    kvb = kv_bytes(spec)
+    ms = res["ms_per_step"]
+    peak, peak_kind = peaks()
+    pk = res["per_kernel"]
+    # dominant kernel: most device time in the attribution pass
+    dom = max(pk.items(), key=lambda kv: kv[1][0])[0] if pk else None
+    dom_ms = pk[dom][0] / pk[dom][1] if dom else None
+    if dom == "decode_split":
+        dom_bytes = decode_kernel_bytes(spec)
+    elif dom == "portable_attention":
+        dom_bytes = kvb + 2 * spec.T * spec.num_q_heads * spec.head_dim * spec.elt_bytes()
+    else:
+        dom_bytes = kvb
+    line = {"value": world * kvb / (ms * 1e-3) / 1e9, "ms_per_step": ms,
+            "tokens_per_s": world * spec.T / (ms * 1e-3),
             "step_ms_median": statistics.median(res["step_ms"]),
             "value_after_write_flush": (world * kvb / (res["alt_ms"] * 1e-3) / 1e9
-                                        if res["alt_ms"] else None),
-            "e2e": {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": res["h2d"],
-                    "d2h_bytes_per_step": res["d2h"]},
-            "gpu_launches": res["launches"],
-            "per_kernel_ms": {k: v[0] / v[1] for k, v in pk.items()},
-            "roofline": roofline, "cpu_baseline": cpu, "clocks": res["clocks"]}
-    if res.get("graph"):
-        line["graph"] = res["graph"]
-    print(json.dumps(line), flush=True)
+                                        if res["alt_ms"] else None)}
+    e2e_ms = res["e2e_ms_per_step"]
+    line["e2e"] = {"value": world * kvb / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                   "ms_per_step": e2e_ms, "h2d_bytes_per_step": res["h2d"],
+                   "d2h_bytes_per_step": res["d2h"], "h2d_copies_per_step": res["h2d_copies"]}
+    line["gpu_launches"] = res["launches"]
+    line["per_kernel_ms"] = {k: v[0] / v[1] for k, v in pk.items()}
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+    line["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                        "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                        "peak_source": f"{peak_kind} HBM copy bandwidth",
+                        "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                        "traffic": recorded_traffic(dom, spec.name) if dom else None}
+    if dom != "decode_split" and "decode_split" in pk:
+        dms = pk["decode_split"][0] / pk["decode_split"][1]
+        db = decode_kernel_bytes(spec)
+        line["roofline_decode"] = {"kernel": "decode_split", "bound": "hbm",
+                                   "achieved": db / (dms * 1e-3) / 1e9, "peak": peak,
+                                   "unit": "GB/s", "frac": db / (dms * 1e-3) / 1e9 / peak,
+                                   "algorithmic_bytes_per_launch": db, "avg_launch_ms": dms}
+    if "prefill_tc" in pk:
+        fl = prefill_flops(spec)
+        pms = pk["prefill_tc"][0] / pk["prefill_tc"][1]
+        tpk, tkind = bf16_peak()
+        ach = fl / (pms * 1e-3) / 1e12
+        line["roofline_prefill"] = {
+            "kernel": "prefill_tile", "bound": "tensor", "achieved": ach, "peak": tpk,
+            "unit": "TFLOP/s", "frac": ach / tpk,
+            "peak_source": f"{tkind} dense bf16 (burst: the kernel is timed alone)",
+            "algorithmic_flops_per_launch": fl, "avg_launch_ms": pms,
+            "traffic": recorded_traffic("prefill_tc", spec.name)}
+    line["clocks"] = res["clocks"]
+    return line
 
 
 if __name__ == "__main__":

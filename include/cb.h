@@ -314,8 +314,9 @@ cb_status cb_read_error_word(void* workspace, int32_t* h_error, void* stream);
  * call's contents; the call clears the part that must start at zero (the error
  * word) on `stream` before its kernels. Calls whose
  * work overlaps on the GPU (other streams, other host threads) race on the
- * array: order them on one stream. The device error word lives in the array,
- * so cb_read_error_word cannot read it for these calls.
+ * array: order them on one stream. The device error word lives in the array:
+ * read it with cb_no_alloc_read_error_word (below) after a call and before the
+ * next one, which clears it.
  */
 #define CB_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 cb_status cb_paged_attention_no_alloc(void* out, const void* q, void* k_cache, void* v_cache,
@@ -329,6 +330,16 @@ cb_status cb_paged_attention_no_alloc(void* out, const void* q, void* k_cache, v
                                       int32_t num_kv_heads, int32_t head_dim, float scale,
                                       int32_t sliding_window, int32_t dtype, uint32_t flags,
                                       void* stream);
+
+/*
+ * cb_no_alloc_read_error_word -- cb_read_error_word for the error word of
+ * cb_paged_attention_no_alloc (which lives in the library's fixed scratch
+ * array, not in a caller's workspace): synchronise `stream`, copy the word of
+ * the current device to *h_error, clear it, and return CB_ERR_DEVICE_CHECK if
+ * it was non-zero. Allocates nothing. The next cb_paged_attention_no_alloc
+ * call clears the word as well, so read it in between.
+ */
+cb_status cb_no_alloc_read_error_word(int32_t* h_error, void* stream);
 
 /* ---- diagnostics (no effect on results) -------------------------------- */
 

@@ -25,7 +25,7 @@ follows these passages:
   (same section). The scatter runs before the attention, because the
   attended range reaches this step's own tokens.
 
-Readings where the pages leave a step open (also listed in the design doc):
+Readings where the pages leave a step open:
 an explicit softmax ``scale``; grouped-query heads map to KV head
 ``h // (Hq // Hkv)``; an optional sliding window keeps the ``W`` most recent
 positions up to and including the query's own; a slot below zero is skipped.
@@ -106,14 +106,6 @@ def gather_request_kv(cache, block_table_row, seq_len, block_size, ring_blocks=0
         blk, off = resolve(block_table_row, p, block_size, ring_blocks)
         out[p] = cache[blk, off]
     return out
-
-
-def request_of_row(query_start_loc, t):
-    """Index of the request whose query rows contain packed row ``t``."""
-    r = 0
-    while not (query_start_loc[r] <= t < query_start_loc[r + 1]):
-        r += 1
-    return r
 
 
 # ---------------------------------------------------------------- attention

@@ -69,6 +69,7 @@ _SIGNATURES = {
         _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _i32, ctypes.c_uint32,
         _vp, ctypes.c_size_t, _vp]),
     "cb_read_error_word": (ctypes.c_int, [_vp, _vp, _vp]),
+    "cb_no_alloc_read_error_word": (ctypes.c_int, [_vp, _vp]),
     "cb_paged_attention_no_alloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
         _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _i32, ctypes.c_uint32,
@@ -322,6 +323,16 @@ def paged_attention_no_alloc(out, q, k_cache, v_cache, query_start_loc, seq_lens
         R, T, NB, BS, Hq, Hkv, D, float(scale), int(sliding_window), _dtype_code(q), int(flags),
         _stream(stream)))
     return out
+
+
+def no_alloc_read_error_word(stream=None) -> int:
+    """Synchronise, return and clear the error word of paged_attention_no_alloc on the
+    current device (0 = no error recorded)."""
+    word = ctypes.c_int32(0)
+    status = lib().cb_no_alloc_read_error_word(ctypes.byref(word), _stream(stream))
+    if status not in (0, 6):
+        _check(status)
+    return int(word.value)
 
 
 def launch_count(kernel: int = -1) -> int:

@@ -492,6 +492,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                       (((c & 7) ^ (key & 7)) << 4)) = new_row;
             uint4* cache = static_cast<uint4*>(lane < kRowChunks ? p.a.k_cache : p.a.v_cache);
             cache[(row_slot * p.a.num_kv_heads + hg * HB + hl) * kRowChunks + c] = new_row;
+            // the producer's next tensor copy into this stage (async proxy) must land
+            // after this ordinary store: order it before the stage's release below
+            fence_proxy_async_smem();
           }
         } else if (row_slot >= num_slots && lane == 0) {
           record_error(p.a.error_word, CB_DEVERR_SLOT_CODE);
@@ -510,6 +513,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           *reinterpret_cast<uint4*>(vs_base + h * box_bytes + (hl * kKB + row) * 128 + c * 16) =
               make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();  // as above: before the stage is handed back to the copies
         __syncwarp();
       }
       // ---- S^T = K Q^T  (16 keys x 8 heads)

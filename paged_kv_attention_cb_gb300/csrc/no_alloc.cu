@@ -66,8 +66,12 @@ extern "C" cb_status cb_paged_attention_no_alloc(
   // must fit in the fixed array.
   const size_t bound = cb_workspace_size(num_requests, num_tokens, num_q_heads, num_kv_heads,
                                          head_dim);
+  // sizes the planner divides by or indexes with are checked first; anything else
+  // malformed is left to cb_paged_attention's validation, which reports it
   const bool plannable = h_query_start_loc != nullptr && h_seq_lens != nullptr &&
-                         num_requests >= 0 && num_q_heads > 0 && num_kv_heads > 0 &&
+                         num_requests >= 0 && num_blocks > 0 && block_size > 0 &&
+                         (block_size & (block_size - 1)) == 0 && block_size <= 256 &&
+                         num_q_heads > 0 && num_kv_heads > 0 &&
                          num_q_heads % num_kv_heads == 0 && (head_dim == 64 || head_dim == 128);
   cb::StepArgs a = {};
   a.num_requests = num_requests;
@@ -103,4 +107,12 @@ extern "C" cb_status cb_paged_attention_no_alloc(
                             h_seq_lens, num_requests, num_tokens, num_blocks, block_size,
                             num_q_heads, num_kv_heads, head_dim, scale, sliding_window, dtype,
                             flags, scratch, bound, stream);
+}
+
+extern "C" cb_status cb_no_alloc_read_error_word(int32_t* h_error, void* stream) {
+  if (!h_error) return cb::report_error(CB_ERR_INVALID_ARG, "null pointer");
+  void* scratch = nullptr;
+  cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) return cb::report_cuda_error(e, "no-alloc scratch address");
+  return cb_read_error_word(scratch, h_error, stream);
 }

@@ -67,18 +67,6 @@ CB_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// Atomic add at GPU scope with acquire-release semantics: the writes this thread has
-// made or observed are visible to a thread that sees the new value, and this thread
-// sees the writes released by the adders before it.
-CB_DEV int atomic_add_acq_rel_gpu(int* ptr, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(reinterpret_cast<uint64_t>(ptr)), "r"(v)
-               : "memory");
-  return old;
-}
-
 // ------------------------------------------------------------------ TMA
 
 CB_DEV void prefetch_tensormap(const CUtensorMap* m) {

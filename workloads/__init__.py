@@ -7,7 +7,8 @@ the per-step metadata the way a scheduler hands it to the attention backend
 implementation": the scheduler builds query_start_loc, seq_lens, slot_mapping
 and block_table before the kernel runs).
 
-Conventions (the readings are listed in the design doc):
+Conventions (readings of what the pages leave open; the cache layout and the query_start_loc
+length follow the same section of "Continuous Batching"):
 
 * q is ``[T, Hq, D]``, k_new/v_new are ``[T, Hkv, D]``, the caches are
   ``[num_blocks, block_size, Hkv, D]`` (K and V in separate tensors).
