@@ -245,6 +245,111 @@ class ClockSampler:
                 "window": window, "reasons": sorted(reasons)}
 
 
+class NvmlClockSampler:
+    """SM clock and throttle reasons read through NVML every PERIOD_S on a background
+    thread, from just before the timed region to just after it, so that even a
+    region of a few milliseconds holds samples. Falls back to ClockSampler (nvidia-smi)
+    where libnvidia-ml cannot be loaded."""
+
+    PERIOD_S = 0.002
+    # nvmlClocksEventReason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        import threading
+
+        self.index = index
+        self.samples = []  # (time, sm_mhz, reasons)
+        self.t0 = self.t1 = None
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._fallback = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            found = False
+            try:  # the CUDA device's own GPU (NVML numbers every GPU of the machine)
+                import torch
+
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(index).uuid)
+                found = self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(),
+                                                            ctypes.byref(self.handle)) == 0
+            except Exception:
+                found = False
+            if not found and self.nvml.nvmlDeviceGetHandleByIndex_v2(
+                    index, ctypes.byref(self.handle)) != 0:
+                raise OSError("no NVML handle")
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except (OSError, AttributeError):
+            self.nvml = None
+            self._fallback = ClockSampler(index)
+
+    def _sample(self):
+        import ctypes
+
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) != 0:
+            return
+        if self.reasons_fn(self.handle, ctypes.byref(rs)) != 0:
+            rs.value = 0
+        self.samples.append((time.perf_counter(), float(mhz.value), int(rs.value)))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.PERIOD_S)
+
+    def __enter__(self):
+        import threading
+
+        if self._fallback is not None:
+            self._fallback.__enter__()
+            return self
+        self._sample()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        self.t0 = time.perf_counter()
+        return self
+
+    def __exit__(self, *exc):
+        if self._fallback is not None:
+            return self._fallback.__exit__(*exc)
+        self.t1 = time.perf_counter()
+        time.sleep(2 * self.PERIOD_S)
+        self._stop.set()
+        self._thread.join(timeout=1.0)
+
+    def summary(self):
+        if self._fallback is not None:
+            return self._fallback.summary()
+        if self.t0 is None or self.t1 is None:
+            return None
+        inside = [x for x in self.samples if self.t0 <= x[0] <= self.t1]
+        window = "inside"
+        if not inside:
+            before = [x for x in self.samples if x[0] < self.t0][-1:]
+            after = [x for x in self.samples if x[0] > self.t1][:1]
+            inside = before + after
+            window = "bracketing (timed region shorter than the sampling period)"
+        if not inside:
+            return None
+        reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[2] & bit})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": self.max_mhz if self.max_mhz else max(x[1] for x in inside),
+                "samples": len(inside), "window": window, "reasons": reasons,
+                "source": f"NVML every {1e3 * self.PERIOD_S:.0f} ms"}
+
+
 # ---------------------------------------------------------------- distributed
 
 
@@ -343,7 +448,7 @@ def run_ours(args, spec, world, rank, local):
     launches0 = cb.launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with NvmlClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             starts[i].record(stream)
@@ -638,7 +743,7 @@ def run_trace_ours(args, cfg, specs, world, rank, local):
     launches0 = cb.launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with NvmlClockSampler(local) as clocks:
         for i in range(n):
             flush_buf.max()  # evicts L2 (clean) between steps
             ev[i][0].record(stream)
@@ -869,7 +974,7 @@ def copy_main(args, world, rank, local):
     launches0 = cb.launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with NvmlClockSampler(local) as clocks:
         for a, b in ev:
             flush_buf.max()
             a.record(stream)

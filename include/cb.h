@@ -64,6 +64,13 @@ typedef enum cb_dtype { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
 
 /* Flags for cb_paged_attention. */
 #define CB_FLAG_PORTABLE_ONLY 0x1u /* run every query row on the portable CUDA-core kernel */
+/* For tests of the failure path only: one wait of each tensor-core attention
+ * kernel (a consumer's first wait) is made to run out after a few polls. The
+ * kernel then records CB_DEVERR_TIMEOUT, stops its other warps, waits for the
+ * copies and products it has in flight, frees its tensor memory and returns;
+ * the step's output is undefined. Call cb_workspace_init before the next step
+ * on that workspace. */
+#define CB_FLAG_TEST_WAIT_EXPIRY 0x2u
 
 /* Error-word codes recorded on the device (bit set). */
 #define CB_DEVERR_BLOCK_ID 0x1 /* a block_table entry outside [0, num_blocks) */

@@ -17,6 +17,7 @@ from .build import LIB_PATH
 CB_F32 = 0
 CB_BF16 = 1
 CB_FLAG_PORTABLE_ONLY = 0x1
+CB_FLAG_TEST_WAIT_EXPIRY = 0x2  # tests of the failure path only (see include/cb.h)
 CB_DEVERR_BLOCK_ID = 0x1
 CB_DEVERR_SLOT = 0x2
 CB_DEVERR_TIMEOUT = 0x4

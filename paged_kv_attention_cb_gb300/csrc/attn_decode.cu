@@ -65,6 +65,7 @@ struct DecodeSmem {
   uint64_t empty[kDecodeMaxStages];
   uint64_t qfull[2];
   uint64_t qempty[2];
+  uint64_t never;  // nothing arrives here: the test hook's wait on it runs out
   SegDesc seg[2];
   long long scan[16];
   long long total_u;
@@ -145,6 +146,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       mbar_init(&sm.qfull[s], 1);
       mbar_init(&sm.qempty[s], HB);
     }
+    mbar_init(&sm.never, 1);
     sm.first_r = -1;
     sm.first_u = 0;
     sm.abort_flag = 0;
@@ -228,14 +230,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int q_row_elems = p.a.num_q_heads * D;
   const uint32_t q_bytes = (uint32_t)(HB * G * D * 2);
 
+  // the producer's counts of query segments published and key blocks issued (read by
+  // its drain after the CTA's final barrier)
+  int prod_k = 0;
+  long long prod_i = 0;
   if (warp == HB) {
     // =================================================== producer warp
     // Request metadata is read 32 requests at a time (lane l holds request
     // wbase + l), and the block-table entries of the next batch of 32 key
     // blocks are requested one batch ahead, so segment switches do not stall
     // the TMA issue on global-memory latency.
-    int k = 0;        // segments published
-    long long i = 0;  // stages issued
+    int& k = prod_k;        // segments published
+    long long& i = prod_i;  // stages issued
     // the KV stream is read once: it leaves L2 first, ahead of the partials that
     // the combine kernel reads back
     const uint64_t kv_policy = l2_policy_evict_first();
@@ -308,7 +314,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const int b_first = cta_of(u_r, U, C);
       const int b_last = cta_of(u_r + units - 1, U, C);
       const int qs = k & 1;
-      if (k >= 2 && !mbar_wait_warp(&sm.qempty[qs], ((k >> 1) - 1) & 1)) { ok = false; break; }
+      if (k >= 2 && !mbar_wait_warp_or_abort(&sm.qempty[qs], ((k >> 1) - 1) & 1, &sm.abort_flag)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) {
         SegDesc& d = sm.seg[qs];
         d.r = r;
@@ -343,7 +352,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           const int pg = __shfl_sync(0xffffffffu, cur, j);
           const int kb = kb_base + j;
           const int s = (int)(i % p.stages);
-          if (i >= p.stages && !mbar_wait_warp(&sm.empty[s], (uint32_t)(((i / p.stages) - 1) & 1))) {
+          if (i >= p.stages && !mbar_wait_warp_or_abort(&sm.empty[s],
+                                                        (uint32_t)(((i / p.stages) - 1) & 1),
+                                                        &sm.abort_flag)) {
             ok = false;
             break;
           }
@@ -402,26 +413,22 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (ok) {
       // terminator
       const int qs = k & 1;
-      if (k >= 2 && !mbar_wait_warp(&sm.qempty[qs], ((k >> 1) - 1) & 1)) ok = false;
+      if (k >= 2 && !mbar_wait_warp_or_abort(&sm.qempty[qs], ((k >> 1) - 1) & 1, &sm.abort_flag))
+        ok = false;
       if (ok && lane == 0) {
         sm.seg[qs].r = -1;
         mbar_arrive(&sm.qfull[qs]);
       }
     }
-    if (!ok) {
-      if (lane == 0) {
-        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
-        sm.abort_flag = 1;
-        // drain the copies this warp issued before leaving
-        const long long first = i > p.stages ? i - p.stages : 0;
-        for (long long j = first; j < i; ++j)
-          mbar_wait(&sm.full[j % p.stages], (uint32_t)((j / p.stages) & 1));
-      }
+    if (!ok && lane == 0) {
+      record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+      set_abort(&sm.abort_flag);
     }
-    return;
-  }
-
+  } else {
   // ===================================================== consumer warps
+  // (a lambda, so that a wait that gives up leaves it with a return and still reaches
+  // the CTA's final barrier)
+  auto consume = [&]() {
   const int hl = warp;  // local KV head
   constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's K (or V) row
   const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
@@ -429,10 +436,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int tq = lane & 3;
   const float sl2 = p.a.scale_log2;
   long long i = 0;
+  if (p.a.test_expire_wait) {
+    // test hook: this warp's first wait runs out (nothing arrives at sm.never)
+    if (!mbar_wait_warp_polls(&sm.never, 0, kTestExpiryPolls)) {
+      if (lane == 0) {
+        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+        set_abort(&sm.abort_flag);
+      }
+      return;
+    }
+  }
   for (int k = 0;; ++k) {
     const int qs = k & 1;
-    if (!mbar_wait_warp(&sm.qfull[qs], (k >> 1) & 1)) {
-      if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
+    if (!mbar_wait_warp_or_abort(&sm.qfull[qs], (k >> 1) & 1, &sm.abort_flag)) {
+      if (lane == 0) {
+        record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+        set_abort(&sm.abort_flag);
+      }
       return;
     }
     const SegDesc d = sm.seg[qs];
@@ -475,8 +495,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     for (int kb = d.kb0; kb < d.kb1; ++kb, ++i) {
       const int s = (int)(i % p.stages);
-      if (!mbar_wait_warp(&sm.full[s], (uint32_t)((i / p.stages) & 1))) {
-        if (lane == 0) { record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE); sm.abort_flag = 1; }
+      if (!mbar_wait_warp_or_abort(&sm.full[s], (uint32_t)((i / p.stages) & 1), &sm.abort_flag)) {
+        if (lane == 0) {
+          record_error(p.a.error_word, CB_DEVERR_TIMEOUT_CODE);
+          set_abort(&sm.abort_flag);
+        }
         return;
       }
       uint8_t* ks_base = stages + s * p.stage_bytes;
@@ -623,6 +646,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (h1 < G) pml[qh_base + h1] = make_float2(m1, l1);
       }
     }
+  }
+  };
+  consume();
+  }
+
+  // Every warp has stopped issuing and waiting. If a wait gave up somewhere in the CTA,
+  // copies the producer issued may not have been consumed: each stage slot and each
+  // query slot has at most one copy in flight, the latest issued into it (a slot is
+  // refilled only after its previous copy was consumed), so waiting for the phase of
+  // the latest copy of each slot drains them all before the shared memory is released.
+  __syncthreads();
+  if (warp == HB && lane == 0 && *reinterpret_cast<volatile int*>(&sm.abort_flag)) {
+    const long long first = prod_i > p.stages ? prod_i - p.stages : 0;
+    for (long long j = first; j < prod_i; ++j)
+      mbar_wait(&sm.full[j % p.stages], (uint32_t)((j / p.stages) & 1));
+    for (int seg = prod_k > 2 ? prod_k - 2 : 0; seg < prod_k; ++seg)
+      mbar_wait(&sm.qfull[seg & 1], (uint32_t)((seg >> 1) & 1));
   }
 }
 

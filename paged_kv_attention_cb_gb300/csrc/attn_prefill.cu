@@ -81,7 +81,10 @@ struct PfBars {
   uint64_t p_full[kTiles];      // P_t in TMEM (the group's four warps)
   uint64_t o_done[kTiles];      // O_t final (its last PV product complete)
   uint64_t drain;
+  uint64_t never;               // nothing arrives here: the test hook's wait on it runs out
   uint32_t tmem_base;
+  int abort;                    // a wait gave up: the other roles stop waiting
+  int issued[kMaxStages];       // ring index of the latest copy issued into each slot
 };
 
 // Ring depth: the shared memory left after the two query tiles, the barriers
@@ -217,6 +220,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     for (int t = 0; t < kTiles; ++t) mbar_init(&bar.o_done[t], 1);
     mbar_init(&bar.drain, 1);
+    mbar_init(&bar.never, 1);
+    bar.abort = 0;
+    for (int s = 0; s < kStages; ++s) bar.issued[s] = -1;
     fence_barrier_init();
   }
   if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_k);
@@ -282,31 +288,27 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     };
     if (p.metadata_ready) grid_dependency_wait();  // the scatter of this step's K/V must be complete
     int ids_cur = tile_pages(0);
-    int issued = 0;  // this warp's tiles issued
     for (int j = 0; j < nkt; ++j) {
       const int i = 2 * j + is_v;
       const int s = i % kStages;
       // the next tile's page ids are read while this one waits for its slot
       const int ids_next = j + 1 < nkt ? tile_pages(j + 1) : 0;
-      if (i >= kStages && !mbar_wait_warp(&bar.empty[s], (uint32_t)(((i / kStages) - 1) & 1))) {
+      if (i >= kStages &&
+          !mbar_wait_warp_or_abort(&bar.empty[s], (uint32_t)(((i / kStages) - 1) & 1), &bar.abort)) {
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bar.full[s], (uint32_t)kTile);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar.full[s], (uint32_t)kTile);
+        bar.issued[s] = i;  // read by the drain after the CTA's final barrier
+      }
       issue_tile(j, ids_cur, sRing + s * kTile, &bar.full[s]);
-      issued = j + 1;
       __syncwarp();
       ids_cur = ids_next;
     }
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
-      // this warp's copies already issued land before the CTA's shared memory is
-      // released (its indices in the last ring's worth: the others were consumed)
-      const int last = 2 * (issued - 1) + is_v;
-      for (int jj = 0; jj < issued; ++jj) {
-        const int ii = 2 * jj + is_v;
-        if (ii > last - kStages) mbar_wait(&bar.full[ii % kStages], (uint32_t)((ii / kStages) & 1));
-      }
+      set_abort(&bar.abort);
     }
   } else if (warp == kWarpMma) {
     // =================================================== MMA issuer
@@ -320,7 +322,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint64_t dK = umma_desc_sw128_base(16, 1024) | (smem_u32(sRing) >> 4);
     const uint64_t dV = umma_desc_sw128_base(kHalfBytes, 1024) | (smem_u32(sRing) >> 4);
     auto slot_ready = [&](int i) {
-      return mbar_wait_warp(&bar.full[i % kStages], (uint32_t)((i / kStages) & 1));
+      return mbar_wait_warp_or_abort(&bar.full[i % kStages], (uint32_t)((i / kStages) & 1),
+                                     &bar.abort);
     };
     // S_t = Q_t K^T with K in ring slot i; its completion is signalled on s_full[t]
     auto qk = [&](int t, int i) {
@@ -341,7 +344,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         umma_bf16_tmem_a_elect(tmem + 2 * kKeys + t * D, tmem + t * kKeys + ks * 8,
                                dv + (uint64_t)(ks * (2048 >> 4)), idO, (acc || ks > 0) ? 1u : 0u);
     };
-    ok = mbar_wait_warp(&bar.q_full, 0) && slot_ready(0);
+    ok = mbar_wait_warp_or_abort(&bar.q_full, 0, &bar.abort) && slot_ready(0);
     if (ok) {
       tcgen05_fence_after();
       qk(0, 0);
@@ -354,7 +357,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const bool more = j + 1 < nkt;
       // the loads are waited for before P, the one wait that depends on the softmax
       if (!slot_ready(iv) || (more && !slot_ready(ik)) ||
-          !mbar_wait_warp(&bar.p_full[0], (uint32_t)(j & 1))) {
+          !mbar_wait_warp_or_abort(&bar.p_full[0], (uint32_t)(j & 1), &bar.abort)) {
         ok = false;
         break;
       }
@@ -364,7 +367,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (!has_b) umma_commit_elect(&bar.empty[iv % kStages]);
       if (more) qk(0, ik);
       if (has_b) {
-        if (!mbar_wait_warp(&bar.p_full[1], (uint32_t)(j & 1))) {
+        if (!mbar_wait_warp_or_abort(&bar.p_full[1], (uint32_t)(j & 1), &bar.abort)) {
           ok = false;
           break;
         }
@@ -376,8 +379,12 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       if (more) umma_commit_elect(&bar.empty[ik % kStages]);
     }
-    if (!ok && lane == 0) record_error(p.a.error_word, 0x4);
-    // every MMA this warp issued has completed before the TMEM is released
+    if (!ok && lane == 0) {
+      record_error(p.a.error_word, 0x4);
+      set_abort(&bar.abort);
+    }
+    // every MMA this warp issued has completed before the TMEM is released (the
+    // commit tracks them all; it completes whether or not the loop ran to its end)
     umma_commit_elect(&bar.drain);
     mbar_wait_warp(&bar.drain, 0);
   } else {
@@ -420,8 +427,11 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const uint32_t tO = tmem + lane_addr + 2 * kKeys + t * D;
       float m_ref = -FLT_MAX;
       float l = 0.f;
-      for (int j = 0; j < nkt; ++j) {
-        if (!mbar_wait_warp(&bar.s_full[t], (uint32_t)(j & 1))) {
+      // test hook: the group's first wait runs out (nothing arrives at bar.never)
+      if (p.a.test_expire_wait && !mbar_wait_warp_polls(&bar.never, 0, kTestExpiryPolls))
+        ok = false;
+      for (int j = 0; j < nkt && ok; ++j) {
+        if (!mbar_wait_warp_or_abort(&bar.s_full[t], (uint32_t)(j & 1), &bar.abort)) {
           ok = false;
           break;
         }
@@ -492,7 +502,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // write the same zeros at the same time), so before either PV reads V.
         if (key_base + kKeys > seq) {
           const int iv = 2 * j + 1;
-          if (!mbar_wait_warp(&bar.full[iv % kStages], (uint32_t)((iv / kStages) & 1))) {
+          if (!mbar_wait_warp_or_abort(&bar.full[iv % kStages], (uint32_t)((iv / kStages) & 1),
+                                       &bar.abort)) {
             ok = false;
             break;
           }
@@ -512,7 +523,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) mbar_arrive(&bar.p_full[t]);
       }
       // ---- epilogue: O / l for the rows of this tile
-      if (ok && !mbar_wait_warp(&bar.o_done[t], 0)) ok = false;
+      if (ok && !mbar_wait_warp_or_abort(&bar.o_done[t], 0, &bar.abort)) ok = false;
       if (ok) {
         tcgen05_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -537,6 +548,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
       } else if (lane == 0) {
         record_error(p.a.error_word, 0x4);
+        set_abort(&bar.abort);
       }
     }
   }
@@ -547,6 +559,16 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (warp == kWarpMma) {
     tcgen05_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // If a wait gave up, copies may be in flight that no MMA consumed. The ring's slots
+  // are filled in index order and a slot is refilled only after its previous copy was
+  // consumed, so only the latest copy of each slot can be in flight: waiting for its
+  // phase drains the ring before the CTA's shared memory is released.
+  if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&bar.abort)) {
+    for (int s2 = 0; s2 < kStages; ++s2) {
+      const int i = bar.issued[s2];
+      if (i >= 0) mbar_wait(&bar.full[s2], (uint32_t)((i / kStages) & 1));
+    }
   }
 }
 

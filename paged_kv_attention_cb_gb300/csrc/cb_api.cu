@@ -295,6 +295,7 @@ cb_status paged_attention_impl(cb_graph_cache* graph, void* out, const void* q, 
   a.scale_log2 = sc * 1.4426950408889634f;
   a.sliding_window = sliding_window > 0 ? sliding_window : 0;
   a.dtype = dtype;
+  a.test_expire_wait = (flags & CB_FLAG_TEST_WAIT_EXPIRY) ? 1 : 0;
   a.error_word = error_word;
 
   cb::Plan plan;

@@ -25,6 +25,7 @@ struct StepArgs {
   float scale_log2;  // softmax scale * log2(e)
   int32_t sliding_window;
   int32_t dtype;     // cb_dtype
+  int32_t test_expire_wait;  // CB_FLAG_TEST_WAIT_EXPIRY: a consumer's first wait runs out
   int32_t* error_word;
 };
 

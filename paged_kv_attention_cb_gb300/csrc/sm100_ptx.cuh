@@ -67,6 +67,35 @@ CB_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Bounded wait that also gives up as soon as another warp of the CTA has set
+// `*abort` (a shared-memory flag): once one role of a pipeline stops, the roles
+// waiting on it stop within a few polls instead of running out their own limit.
+CB_DEV bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const int* abort) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 7) == 7 && *reinterpret_cast<const volatile int*>(abort) != 0) return false;
+  }
+  return false;
+}
+
+CB_DEV bool mbar_wait_warp_or_abort(uint64_t* bar, uint32_t parity, const int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort));
+}
+
+// A wait with a short, given limit, for the test hook that makes one wait of a
+// kernel run out: it waits on a barrier nothing arrives at, so it always fails.
+CB_DEV bool mbar_wait_warp_polls(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  bool ok = false;
+  for (uint32_t i = 0; i < polls && !ok; ++i) ok = mbar_try_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Polls of the test hook's wait (a few microseconds).
+constexpr uint32_t kTestExpiryPolls = 64;
+
+// Set the CTA's abort flag (read by mbar_wait_or_abort in the other warps).
+CB_DEV void set_abort(int* abort) { *reinterpret_cast<volatile int*>(abort) = 1; }
+
 // ------------------------------------------------------------------ TMA
 
 CB_DEV void prefetch_tensormap(const CUtensorMap* m) {
