@@ -58,7 +58,8 @@ constexpr int kSoftmaxThreads = kTiles * kRows;
 constexpr int kWarpTma = kSoftmaxThreads / 32;
 constexpr int kWarpMma = kWarpTma + 1;
 constexpr int kWarpTmaV = kWarpMma + 1;  // kWarpTma loads K tiles, kWarpTmaV V tiles
-constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kWarpScatter = kWarpTmaV + 1;  // writes the CTA's new K/V rows to the cache
+constexpr int kThreads = kSoftmaxThreads + 128;
 // Register bound: up to three warps share each SM sub-partition's 16K registers,
 // so a thread may hold at most 168; a 384-thread launch bound makes the compiler keep to it.
 constexpr int kThreadsBound = 384;
@@ -128,6 +129,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsBound, 1)
 prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_kn,
+                    const __grid_constant__ CUtensorMap tmap_vn,
                     const __grid_constant__ PrefillArgs p) {
   static_assert(D == 64 || D == 128, "head_dim");
   constexpr int kHalves = D / 64;
@@ -225,14 +228,20 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int s = 0; s < kStages; ++s) bar.issued[s] = -1;
     fence_barrier_init();
   }
-  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_k);
-  if (warp == kWarpTmaV && lane == 0) prefetch_tensormap(&tmap_v);
+  if (warp == kWarpTma && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    if (p.k_new != nullptr) prefetch_tensormap(&tmap_kn);
+  }
+  if (warp == kWarpTmaV && lane == 0) {
+    prefetch_tensormap(&tmap_v);
+    if (p.k_new != nullptr) prefetch_tensormap(&tmap_vn);
+  }
   if (warp == kWarpMma) tmem_alloc(&bar.tmem_base, kTmemCols);
   // q and the metadata were written before the step's first kernel. When that
   // kernel is one of libcb's (which start their dependents only after their own
   // wait on the previous grid), they are visible already and only the cache
-  // reads (the TMA warp) wait for the scatter; otherwise every thread waits.
-  if (!p.metadata_ready) grid_dependency_wait();
+  // reads (the TMA warps) wait for a scatter launch; otherwise every thread waits.
+  if (!p.metadata_ready && !p.concurrent) grid_dependency_wait();
   tcgen05_fence_before();
   __syncthreads();
   tcgen05_fence_after();
@@ -256,8 +265,16 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // fall behind the tensor pipe.
     const int is_v = warp == kWarpTmaV;
     const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+    const CUtensorMap* nmap = is_v ? &tmap_vn : &tmap_kn;
+    const uint4* new_rows = static_cast<const uint4*>(is_v ? p.v_new : p.k_new);
+    const uint4* cache = static_cast<const uint4*>(is_v ? p.a.v_cache : p.a.k_cache);
+    const bool fuse = p.k_new != nullptr;
     const int BS = p.a.block_size;
+    const int Hkv = p.a.num_kv_heads;
     const int box = p.box_keys;
+    const int lg_box = __ffs(box) - 1;  // box and block_size are powers of two
+    const int lg_bs = __ffs(BS) - 1;
+    const int bs_mask = BS - 1;
     const int ppt = kKeys / box;  // pages per key tile
     const int nbox = ppt * kHalves;
     const int npages_req = (seq + BS - 1) / BS;
@@ -265,46 +282,149 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // page ids of key tile j (lane i < ppt: page i of the tile); checked where
     // they are used, so that the load of the next tile's ids does not stall
     auto tile_pages = [&](int j) -> int {
-      const int lp = (kt0 + j) * kKeys / BS + lane;
+      const int lp = (((kt0 + j) * kKeys) >> lg_bs) + lane;
       return (lane < ppt && lp < npages_req) ? __ldg(bt + bt_entry(lp, p.a.ring_blocks)) : 0;
     };
-    // key tile j into `dst`: lane i loads box i (page i / kHalves, half i % kHalves
-    // of head_dim); a page past the request, or past the pool, reads as zeros
-    auto issue_tile = [&](int j, int pg, uint8_t* dst, uint64_t* full) {
-      const int key0 = BS > kKeys ? ((kt0 + j) * kKeys) % BS : 0;
-      const int page = lane / kHalves;
-      const int half = lane % kHalves;
-      int pgb = __shfl_sync(0xffffffffu, pg, page & 31);
-      __syncwarp();  // the expect_tx is registered first
-      if (lane < nbox) {
-        if ((kt0 + j) * kKeys / BS + page >= npages_req) {
-          pgb = p.a.num_blocks;
-        } else if (pgb < 0 || pgb >= p.a.num_blocks) {
-          record_error(p.a.error_word, 0x1);
-          pgb = p.a.num_blocks;
-        }
-        tma_load_4d(dst + half * kHalfBytes + page * box * 128, map, full, half * 64, key0, g, pgb);
+    // slot_mapping entries of tile j's keys lane + 32 q that are this step's new
+    // positions (ctx <= pos < seq); -1 elsewhere
+    auto tile_slots = [&](int j, long long (&sl)[4]) {
+      const int key_base = (kt0 + j) * kKeys;
+      if (!(fuse && key_base + kKeys > ctx && key_base < seq)) return;  // no new position
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int pos = key_base + lane + 32 * q4;
+        sl[q4] = (pos >= ctx && pos < seq) ? __ldg(p.slot_mapping + q_start + (pos - ctx)) : -1;
       }
     };
-    if (p.metadata_ready) grid_dependency_wait();  // the scatter of this step's K/V must be complete
+    if (p.metadata_ready && !p.concurrent) grid_dependency_wait();  // the step's scatter launch
     int ids_cur = tile_pages(0);
+    long long sl_cur[4], sl_next[4];
+    tile_slots(0, sl_cur);
     for (int j = 0; j < nkt; ++j) {
       const int i = 2 * j + is_v;
       const int s = i % kStages;
-      // the next tile's page ids are read while this one waits for its slot
+      uint8_t* dst = sRing + s * kTile;
+      const int key_base = (kt0 + j) * kKeys;
+      // the next tile's page ids and slots are read while this one waits for its slot
       const int ids_next = j + 1 < nkt ? tile_pages(j + 1) : 0;
+      if (j + 1 < nkt) tile_slots(j + 1, sl_next);
       if (i >= kStages &&
           !mbar_wait_warp_or_abort(&bar.empty[s], (uint32_t)(((i / kStages) - 1) & 1), &bar.abort)) {
         ok = false;
         break;
       }
+      // ---- where each page box of the tile comes from. A new position (ctx <= pos <
+      // seq) whose slot is its own holds k_new's row after this step, so it is read from
+      // k_new; any other position from the cache (not written in this step). Tiles of
+      // context only (the common case) skip the test: this warp's issue rate bounds the
+      // ring's refill rate.
+      const bool tile_new = fuse && key_base + kKeys > ctx && key_base < seq;  // warp-uniform
+      unsigned bad[4] = {0u, 0u, 0u, 0u};  // bit kk: key key_base + kk is new, slot not its own
+      int src = 0;  // lane i < ppt: page i from 0: the cache (or zeros past the request),
+                    // 1: a box of k_new rows, 2: row by row (straddles ctx or foreign slot)
+      unsigned gen = 0u;
+      if (tile_new) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int kk = lane + 32 * q4;
+          const int pos = key_base + kk;
+          const int pgk = __shfl_sync(0xffffffffu, ids_cur, (kk >> lg_box) & 31);
+          const bool isnew = pos >= ctx && pos < seq;
+          bad[q4] = __ballot_sync(0xffffffffu,
+                                  isnew && sl_cur[q4] != (long long)pgk * BS + (pos & bs_mask));
+        }
+        const int kp = key_base + (lane << lg_box);
+        if (lane < ppt && kp < seq && kp + box > ctx) {
+          bool pbad = false;
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const int lo = max(lane << lg_box, 32 * w4), hi = min((lane << lg_box) + box, 32 * w4 + 32);
+            if (lo < hi) {
+              const unsigned bits = bad[w4] >> (lo - 32 * w4);
+              pbad |= (hi - lo == 32 ? bits : (bits & ((1u << (hi - lo)) - 1u))) != 0u;
+            }
+          }
+          src = (kp >= ctx && !pbad) ? 1 : 2;
+        }
+        gen = __ballot_sync(0xffffffffu, src == 2);
+      }
+      if (gen != 0u) {
+        // row by row: 16-byte chunks e = lane + 32 m of (row, half, chunk), loads first
+        constexpr int kBatch = 8;
+        for (unsigned m = gen; m != 0u; m &= m - 1u) {
+          const int pi = __ffs(m) - 1;
+          const int pg = __shfl_sync(0xffffffffu, ids_cur, pi);
+          const int kpi = key_base + pi * box;
+          const bool pg_ok = pg >= 0 && pg < p.a.num_blocks;
+          const int nchunks = box * kHalves * 8;
+          for (int e0 = 0; e0 < nchunks; e0 += 32 * kBatch) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+              const int e = e0 + lane + 32 * u;
+              const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+              const int pos = kpi + row;
+              v[u] = make_uint4(0u, 0u, 0u, 0u);
+              if (e < nchunks && pos < seq) {
+                const int kk = pos - key_base;
+                const unsigned bw = kk < 32 ? bad[0] : kk < 64 ? bad[1] : kk < 96 ? bad[2] : bad[3];
+                const bool own = pos >= ctx && ((bw >> (kk & 31)) & 1u) == 0u;
+                if (own) {
+                  v[u] = __ldg(new_rows + (((long long)(q_start + pos - ctx) * Hkv + g) * D + h * 64) / 8 + c);
+                } else if (pg_ok) {
+                  v[u] = __ldg(cache + (((long long)pg * BS + (pos & bs_mask)) * Hkv + g) * (D / 8) + h * 8 + c);
+                } else if (c == 0 && h == 0) {
+                  record_error(p.a.error_word, 0x1);
+                }
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+              const int e = e0 + lane + 32 * u;
+              const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+              const int trow = pi * box + row;  // row within the tile
+              if (e < nchunks)
+                *reinterpret_cast<uint4*>(dst + h * kHalfBytes + trow * 128 + ((c ^ (trow & 7)) << 4)) = v[u];
+            }
+          }
+        }
+        // the tensor cores read these rows through the async proxy
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar.full[s], (uint32_t)kTile);
+        const int tma_bytes = kTile - __popc(gen) * kHalves * box * 128;
+        mbar_arrive_expect_tx(&bar.full[s], (uint32_t)tma_bytes);
         bar.issued[s] = i;  // read by the drain after the CTA's final barrier
       }
-      issue_tile(j, ids_cur, sRing + s * kTile, &bar.full[s]);
+      __syncwarp();  // the expect_tx is registered first
+      {
+        // lane b < nbox loads box b (page b / kHalves, half b % kHalves of head_dim); a
+        // page past the request, or past the pool, reads as zeros
+        const int key0 = BS > kKeys ? (key_base & bs_mask) : 0;
+        const int page = lane / kHalves;
+        const int half = lane % kHalves;
+        int pgb = __shfl_sync(0xffffffffu, ids_cur, page & 31);
+        const int srcb = tile_new ? __shfl_sync(0xffffffffu, src, page & 31) : 0;
+        if (lane < nbox && srcb != 2) {
+          uint8_t* bdst = dst + half * kHalfBytes + page * box * 128;
+          if (srcb == 1) {
+            tma_load_3d(bdst, nmap, &bar.full[s], half * 64, g, q_start + (key_base + (page << lg_box) - ctx));
+          } else {
+            if ((((kt0 + j) * kKeys) >> lg_bs) + page >= npages_req) {
+              pgb = p.a.num_blocks;
+            } else if (pgb < 0 || pgb >= p.a.num_blocks) {
+              record_error(p.a.error_word, 0x1);
+              pgb = p.a.num_blocks;
+            }
+            tma_load_4d(bdst, map, &bar.full[s], half * 64, key0, g, pgb);
+          }
+        }
+      }
       __syncwarp();
       ids_cur = ids_next;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) sl_cur[q4] = sl_next[q4];
     }
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
@@ -387,6 +507,50 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // commit tracks them all; it completes whether or not the loop ran to its end)
     umma_commit_elect(&bar.drain);
     mbar_wait_warp(&bar.drain, 0);
+  } else if (warp == kWarpScatter) {
+    // =================================================== scatter warp
+    // The new K and V rows of this CTA's tokens for KV head g go to their slots
+    // (a slot below zero is skipped, one past the pool recorded and skipped). The
+    // tile pairs of all KV heads cover every (token, head) of the request once.
+    // Nothing in the step reads these positions from the cache (the TMA warps read
+    // them from k_new), so the writes need no ordering with the rest of the CTA.
+    if (p.k_new != nullptr) {
+      constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
+      constexpr int kPerTok = 2 * kRowChunks;
+      const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
+      const int Hkv = p.a.num_kv_heads;
+      const int n = (cta_tok_end - cta_tok0) * kPerTok;
+      constexpr int kBatch = 4;
+      for (int e0 = 0; e0 < n; e0 += 32 * kBatch) {
+        uint4 v[kBatch];
+        long long sl[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + lane + 32 * u;
+          sl[u] = -1;
+          if (e < n) {
+            const int tok = q_start + cta_tok0 + e / kPerTok;
+            const int rem = e % kPerTok;
+            const uint4* src = static_cast<const uint4*>(rem < kRowChunks ? p.k_new : p.v_new);
+            sl[u] = __ldg(p.slot_mapping + tok);
+            v[u] = __ldg(src + ((long long)tok * Hkv + g) * kRowChunks + rem % kRowChunks);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = e0 + lane + 32 * u;
+          if (e < n && sl[u] >= 0) {
+            const int rem = e % kPerTok;
+            if (sl[u] < num_slots) {
+              uint4* dstc = static_cast<uint4*>(rem < kRowChunks ? p.a.k_cache : p.a.v_cache);
+              dstc[(sl[u] * Hkv + g) * kRowChunks + rem % kRowChunks] = v[u];
+            } else if (rem == 0) {
+              record_error(p.a.error_word, 0x2);
+            }
+          }
+        }
+      }
+    }
   } else {
     // =================================================== softmax warpgroups
     const int t = warp >> 2;             // query tile of this group
@@ -570,6 +734,15 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (i >= 0) mbar_wait(&bar.full[s2], (uint32_t)((i / kStages) & 1));
     }
   }
+  // Launched beside the decode kernel: the last CTA to finish waits for the decode
+  // grid, so that this grid completes only after it (the combine launch that follows
+  // waits for this grid and reads the decode partials), and resets the counter.
+  if (p.concurrent && threadIdx.x == 0) {
+    if (atomicAdd(p.exit_counter, 1) == p.total_ctas - 1) {
+      atomicExch(p.exit_counter, 0);
+      grid_dependency_wait();
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -615,6 +788,17 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
   err = encode(&mk, a.k_cache, 4, cd, cs, cb_);
   if (err == cudaSuccess) err = encode(&mv, a.v_cache, 4, cd, cs, cb_);
   if (err != cudaSuccess) return err;
+  // the step's new rows [T, Hkv, D] as (d, head, token); box: 64 of d, one head,
+  // box_keys tokens -- the same shared-memory rows as a page box of the cache
+  CUtensorMap mkn = mk, mvn = mv;  // unused without new rows
+  if (p.k_new != nullptr) {
+    cuuint64_t nd[3] = {(cuuint64_t)D, (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.num_tokens};
+    cuuint64_t ns[2] = {(cuuint64_t)D * e, (cuuint64_t)a.num_kv_heads * D * e};
+    cuuint32_t nb[3] = {64, 1, (cuuint32_t)p.box_keys};
+    err = encode(&mkn, const_cast<void*>(p.k_new), 3, nd, ns, nb);
+    if (err == cudaSuccess) err = encode(&mvn, const_cast<void*>(p.v_new), 3, nd, ns, nb);
+    if (err != cudaSuccess) return err;
+  }
   auto kern = prefill_tile_kernel<D>;
   static bool attr_set = false;
   constexpr size_t smem = smem_bytes<D>();
@@ -623,7 +807,8 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mk, mv, p);
+  return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mk, mv, mkn,
+                    mvn, p);
 }
 
 }  // namespace

@@ -5,6 +5,8 @@
 // go to the split-KV kernel with a byte-balanced partition, prefill rows to
 // the prefill kernel, and whatever the fast kernels do not cover to the
 // portable kernel.
+#include <stdlib.h>
+
 #include <algorithm>
 #include <utility>
 #include <vector>
@@ -98,10 +100,37 @@ size_t workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_q_h
   return layout(num_requests, num_q_heads, num_kv_heads, head_dim).total;
 }
 
+// SMs left to the prefill kernel while the decode kernel streams (concurrent mixed
+// step). Model, from measurements of the two kernels side by side on GB300: the decode
+// stream runs at min(HBM, C x per-SM rate) on its C SMs; the prefill tiles run at a
+// fixed rate per SM, on k SMs until the decode grid finishes and on every SM after
+// that. The share minimises the modelled step time (ties: more SMs for the decode).
+// CB_PREFILL_SMS overrides it (for measurements).
+int prefill_sm_share(long long decode_bytes, double prefill_flops, int n_prefill_ctas, int S) {
+  const int kmax = std::max(1, std::min(n_prefill_ctas, S - 1));
+  const char* env = getenv("CB_PREFILL_SMS");
+  if (env != nullptr && *env != '\0') return std::max(1, std::min(atoi(env), kmax));
+  constexpr double kHbm = 6.6e12;          // B/s, decode stream on enough SMs
+  constexpr double kHbmPerSm = 75e9;       // B/s, decode stream per SM
+  constexpr double kFlopsPerSm = 6.0e12;   // causal-pair FLOP/s of prefill tiles per SM
+  int best_k = 1;
+  double best_t = 1e30;
+  for (int k = 1; k <= kmax; ++k) {
+    const double td = (double)decode_bytes / std::min(kHbm, (S - k) * kHbmPerSm);
+    const double done = k * kFlopsPerSm * td;  // prefill work finished beside the decode
+    const double t = done >= prefill_flops ? std::max(td, prefill_flops / (k * kFlopsPerSm))
+                                           : td + (prefill_flops - done) / (S * kFlopsPerSm);
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
+      best_k = k;
+    }
+  }
+  return best_k;
+}
+
 void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_t* h_seq_lens,
                uint32_t flags, const ScatterInputs* scatter, void* workspace,
                size_t workspace_bytes) {
-  bool scatter_first = scatter != nullptr;
   plan.workspace = workspace;
   plan.workspace_bytes = workspace_bytes;
   plan.fast_decode = false;
@@ -110,53 +139,135 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   plan.portable_mode = 0;
   plan.has_combine = false;
   plan.fused_scatter = false;
+  plan.concurrent = false;
   if ((flags & CB_FLAG_PORTABLE_ONLY) || a.dtype == CB_F32) return;
 
   // ---- which rows exist
   long long U = 0;
   bool has_prefill = false;
+  double flops = 0.0;  // prefill: causal (query, key) pairs x 4 Hq D
   for (int r = 0; r < a.num_requests; ++r) {
     const int ql = h_qsl[r + 1] - h_qsl[r];
-    if (ql == 1 && h_seq_lens[r] > 0) U += decode_units_host(h_seq_lens[r], a.sliding_window);
-    else if (ql > 1) has_prefill = true;
+    if (ql == 1 && h_seq_lens[r] > 0) {
+      U += decode_units_host(h_seq_lens[r], a.sliding_window);
+    } else if (ql > 1) {
+      has_prefill = true;
+      const long long ctx = h_seq_lens[r] - ql;
+      long long pairs = 0;
+      if (a.sliding_window > 0) {
+        for (int i = 0; i < ql; ++i) pairs += std::min<long long>(ctx + i + 1, a.sliding_window);
+      } else {
+        pairs = (long long)ql * ctx + (long long)ql * (ql + 1) / 2;
+      }
+      flops += 4.0 * a.num_q_heads * a.head_dim * (double)pairs;
+    }
   }
 
-  // ---- decode rows: split-KV kernel
+  // ---- which kernels can take them
   const int G = a.num_q_heads / a.num_kv_heads;
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
-  const bool decode_ok = U > 0 && a.block_size % 16 == 0 && G <= 8 &&
-                         a.num_kv_heads % HB == 0;
+  const bool decode_ok = U > 0 && a.block_size % 16 == 0 && G <= 8 && a.num_kv_heads % HB == 0;
+  // a 128-key tile is made of whole page boxes (block_size divides 128) or lies
+  // inside one page (block_size a multiple of 128)
+  const bool tile_pages_ok = a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
+  std::vector<std::pair<long long, int>> order;  // prefill requests (weight, r), heaviest first
+  if (has_prefill && tile_pages_ok && G <= 16 && kRowsPerTile % G == 0) {
+    for (int r = 0; r < a.num_requests; ++r) {
+      const int ql = h_qsl[r + 1] - h_qsl[r];
+      if (ql > 1) order.emplace_back(-(long long)h_seq_lens[r] * ql, r);
+    }
+    std::stable_sort(order.begin(), order.end());
+  }
+  const int n_launch = (int)((order.size() + kPrefillMaxEntries - 1) / kPrefillMaxEntries);
+  const bool prefill_ok = !order.empty() && n_launch <= kMaxPrefillLaunches;
+  DecodeArgs& d = plan.decode;
   if (decode_ok) {
-    DecodeArgs& d = plan.decode;
-    d.a = a;
-    d.heads_per_cta = HB;
-    d.total_units = U;
-    d.num_ctas = (int)std::min<long long>(std::min(sm_count(), kMaxDecodeCtas), U);
     d.stage_bytes = 2 * (a.head_dim / 64) * HB * 16 * 128;
     d.q_slot_bytes = HB * G * a.head_dim * 2;
     const size_t fixed = decode_smem_bytes(0, d.stage_bytes, d.q_slot_bytes);
     d.stages = (int)std::min<size_t>(kDecodeMaxStages, (kDecodeSmemLimit - fixed) / d.stage_bytes);
+    plan.fast_decode = d.stages >= 2;
+  }
+  plan.fast_prefill = prefill_ok;
+  if (plan.fast_decode && plan.fast_prefill) plan.portable_mode = -1;
+  else if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
+  else if (plan.fast_prefill) plan.portable_mode = U > 0 ? 1 : -1;
+  // Every row on a tensor-core kernel (one prefill launch at most): the kernels write the
+  // step's new rows themselves and read the step's own positions from k_new / v_new, so
+  // there is no scatter launch; a step with both kinds of rows runs the prefill grid
+  // beside the decode grid, on the SMs the decode grid leaves.
+  plan.fused_scatter = scatter != nullptr && plan.portable_mode == -1 && n_launch <= 1;
+  plan.concurrent = plan.fused_scatter && plan.fast_decode && plan.fast_prefill;
+  const bool scatter_first = scatter != nullptr && !plan.fused_scatter;
+
+  // ---- prefill rows: tcgen05 tile kernel, heaviest requests first
+  int prefill_total_ctas = 0;
+  if (plan.fast_prefill) {
+    const int TQ = kRowsPerTile / G;
+    for (int l = 0; l < n_launch; ++l) {
+      PrefillArgs& pa = plan.prefill[l];
+      pa.a = a;
+      pa.tile_tokens = TQ;
+      pa.box_keys = std::min(a.block_size, 128);
+      pa.n_entries = 0;
+      // the scatter, the decode kernel or an earlier prefill launch runs first
+      pa.metadata_ready = (scatter_first || plan.fast_decode || l > 0) ? 1 : 0;
+      pa.device_work = 0;
+      pa.total_ctas = 0;
+      pa.k_new = plan.fused_scatter ? scatter->k_new : nullptr;
+      pa.v_new = plan.fused_scatter ? scatter->v_new : nullptr;
+      pa.slot_mapping = plan.fused_scatter ? scatter->slot_mapping : nullptr;
+      pa.concurrent = plan.concurrent ? 1 : 0;
+      pa.exit_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kExitCounterOffset);
+      for (size_t i = (size_t)l * kPrefillMaxEntries;
+           i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
+        const int r = order[i].second;
+        const int ql = h_qsl[r + 1] - h_qsl[r];
+        PrefillEntry& e = pa.entries[pa.n_entries++];
+        e.r = r;
+        e.n_qtiles = (ql + TQ - 1) / TQ;
+        e.q_start = h_qsl[r];
+        e.q_len = ql;
+        e.seq_len = h_seq_lens[r];
+        pa.total_ctas += prefill_ctas(e.n_qtiles, a.num_kv_heads);
+      }
+      prefill_total_ctas += pa.total_ctas;
+    }
+    plan.n_prefill_launches = n_launch;
+  }
+
+  // ---- decode rows: split-KV kernel
+  if (plan.fast_decode) {
+    d.a = a;
+    d.heads_per_cta = HB;
+    d.total_units = U;
+    int C = std::min(sm_count(), kMaxDecodeCtas);
+    if (plan.concurrent) {
+      const long long bytes = U * 16LL * 2 * a.num_kv_heads * a.head_dim * 2;
+      C = sm_count() - prefill_sm_share(bytes, flops, prefill_total_ctas, sm_count());
+    }
+    d.num_ctas = (int)std::min<long long>(C, U);
     d.units_on_device = 0;
-    // a step of decode rows only: each row's new K/V is written by the CTA that
-    // reads the request's last key block (the decode kernel is the step's first)
-    d.fuse_scatter = scatter != nullptr && !has_prefill ? 1 : 0;
+    // each decode row's new K/V is written by the CTA that reads the request's last key
+    // block (the decode kernel is then the step's first)
+    d.fuse_scatter = plan.fused_scatter ? 1 : 0;
     d.k_new = scatter ? scatter->k_new : nullptr;
     d.v_new = scatter ? scatter->v_new : nullptr;
     d.slot_mapping = scatter ? scatter->slot_mapping : nullptr;
-    d.metadata_ready = scatter_first && !d.fuse_scatter ? 1 : 0;
+    d.metadata_ready = scatter_first ? 1 : 0;
     // where each CTA's range [b*U/C, (b+1)*U/C) starts: (request, its first unit)
     d.has_table = d.num_ctas <= kDecodeTableCtas;
     if (d.has_table) {
       long long u = 0;
       int b = 0;
-      const long long C = d.num_ctas;
+      const long long Cn = d.num_ctas;
       for (int r = 0; r < a.num_requests && b < d.num_ctas; ++r) {
         const int ql = h_qsl[r + 1] - h_qsl[r];
         if (ql != 1 || h_seq_lens[r] <= 0) continue;
         const int units = decode_units_host(h_seq_lens[r], a.sliding_window);
         const int kbl = kb_lo_host(h_seq_lens[r], a.sliding_window);
-        while (b < d.num_ctas && (long long)b * U / C < u + units) {
-          const long long lo = (long long)b * U / C, hi = (long long)(b + 1) * U / C;
+        while (b < d.num_ctas && (long long)b * U / Cn < u + units) {
+          const long long lo = (long long)b * U / Cn, hi = (long long)(b + 1) * U / Cn;
           d.cta_first[b] = DecodeCtaStart{r, (int)u, kbl + (int)(lo - u),
                                           kbl + (int)(std::min(u + units, hi) - u), h_qsl[r],
                                           h_seq_lens[r]};
@@ -171,10 +282,6 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
     d.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     d.part_o = reinterpret_cast<float*>(ws + w.part_o);
     plan.decode_plan.smem_bytes = decode_smem_bytes(d.stages, d.stage_bytes, d.q_slot_bytes);
-    if (d.stages >= 2) plan.fast_decode = true;
-    if (!plan.fast_decode) d.fuse_scatter = 0;
-    plan.fused_scatter = d.fuse_scatter != 0;
-    if (plan.fused_scatter) scatter_first = false;
     // the requests split over several CTAs, merged by the combine launch
     CombineArgs& c = plan.combine;
     combine_common(c, a, d);
@@ -195,54 +302,8 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
       c.entries[c.n_entries++] = CombineEntry{r, h_qsl[r], b0, b1 - b0 + 1};
     }
     c.kv_per_cta = combine_kv_per_cta(a, c.n_entries >= 0 ? c.n_entries : a.num_requests);
-    plan.has_combine = plan.fast_decode && c.n_entries != 0;
+    plan.has_combine = c.n_entries != 0;
   }
-
-  // ---- prefill rows: tcgen05 tile kernel, heaviest requests first
-  // a 128-key tile is made of whole page boxes (block_size divides 128) or lies
-  // inside one page (block_size a multiple of 128)
-  const bool tile_pages_ok = a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
-  const bool prefill_ok = has_prefill && tile_pages_ok && G <= 16 && kRowsPerTile % G == 0;
-  if (prefill_ok) {
-    const int TQ = kRowsPerTile / G;
-    std::vector<std::pair<long long, int>> order;  // (weight, r)
-    for (int r = 0; r < a.num_requests; ++r) {
-      const int ql = h_qsl[r + 1] - h_qsl[r];
-      if (ql > 1) order.emplace_back(-(long long)h_seq_lens[r] * ql, r);
-    }
-    std::stable_sort(order.begin(), order.end());
-    const int n_launch = (int)((order.size() + kPrefillMaxEntries - 1) / kPrefillMaxEntries);
-    if (n_launch <= kMaxPrefillLaunches) {
-      for (int l = 0; l < n_launch; ++l) {
-        PrefillArgs& pa = plan.prefill[l];
-        pa.a = a;
-        pa.tile_tokens = TQ;
-        pa.box_keys = std::min(a.block_size, 128);
-        pa.n_entries = 0;
-        // the scatter, the decode kernel or an earlier prefill launch runs first
-        pa.metadata_ready = (scatter_first || plan.fast_decode || l > 0) ? 1 : 0;
-        pa.device_work = 0;
-        pa.total_ctas = 0;
-        for (size_t i = (size_t)l * kPrefillMaxEntries;
-             i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
-          const int r = order[i].second;
-          const int ql = h_qsl[r + 1] - h_qsl[r];
-          PrefillEntry& e = pa.entries[pa.n_entries++];
-          e.r = r;
-          e.n_qtiles = (ql + TQ - 1) / TQ;
-          e.q_start = h_qsl[r];
-          e.q_len = ql;
-          e.seq_len = h_seq_lens[r];
-          pa.total_ctas += prefill_ctas(e.n_qtiles, a.num_kv_heads);
-        }
-      }
-      plan.n_prefill_launches = n_launch;
-      plan.fast_prefill = true;
-    }
-  }
-  if (plan.fast_decode && plan.fast_prefill) plan.portable_mode = -1;
-  else if (plan.fast_decode) plan.portable_mode = has_prefill ? 2 : -1;
-  else if (plan.fast_prefill) plan.portable_mode = U > 0 ? 1 : -1;
 }
 
 bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_prefill,
@@ -255,6 +316,7 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   plan.portable_mode = -1;
   plan.has_combine = false;
   plan.fused_scatter = false;
+  plan.concurrent = false;
   if (a.dtype != CB_BF16) return false;
   const int G = a.num_q_heads / a.num_kv_heads;
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
@@ -296,6 +358,10 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   pa.box_keys = std::min(a.block_size, 128);
   pa.n_entries = 0;
   pa.metadata_ready = 0;
+  pa.k_new = pa.v_new = nullptr;  // the captured scatter launch writes the rows first
+  pa.slot_mapping = nullptr;
+  pa.concurrent = 0;
+  pa.exit_counter = nullptr;
   pa.device_work = 1;
   pa.total_ctas = prefill_ctas_bound(a.num_tokens, a.num_requests, pa.tile_tokens,
                                      a.num_kv_heads);
@@ -321,10 +387,17 @@ size_t workspace_extent(const Plan& plan, const StepArgs& a) {
 size_t workspace_zeroed_prefix(const StepArgs& a, size_t workspace_bytes) {
   (void)a;
   (void)workspace_bytes;
-  return kWorkspaceHeaderBytes;  // the error word
+  return kWorkspaceHeaderBytes;  // the error word and the prefill exit counter
 }
 
 cudaError_t run_plan(const Plan& plan, const StepArgs& a, cudaStream_t stream) {
+  if (plan.concurrent) {
+    // decode grid, the prefill grid beside it, then the merge of the split requests
+    cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);
+    if (e == cudaSuccess) e = launch_prefill(plan.prefill[0], stream);
+    if (e == cudaSuccess && plan.has_combine) e = launch_decode_combine(plan.combine, stream);
+    return e;
+  }
   if (plan.fast_decode) {
     cudaError_t e = launch_decode(plan.decode, plan.decode_plan, stream);
     if (e == cudaSuccess && plan.has_combine) e = launch_decode_combine(plan.combine, stream);

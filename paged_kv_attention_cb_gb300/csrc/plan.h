@@ -11,7 +11,8 @@
 
 namespace cb {
 
-constexpr size_t kWorkspaceHeaderBytes = 256;  // error word + reserved
+constexpr size_t kWorkspaceHeaderBytes = 256;  // error word, prefill exit counter, reserved
+constexpr size_t kExitCounterOffset = 64;      // int: prefill CTAs finished (zero between steps)
 constexpr int kMaxDecodeCtas = 2048;           // upper bound on decode CTAs (workspace sizing)
 constexpr int kMaxPrefillLaunches = 8;         // x kPrefillMaxEntries prefill requests per step
 
@@ -29,7 +30,8 @@ struct Plan {
   int portable_mode;   // -1: none, 0: all rows, 1: decode rows, 2: prefill rows
   bool fast_decode;    // decode rows on the split-KV tensor-core kernel
   bool fast_prefill;   // prefill rows on the tcgen05 tile kernel
-  bool fused_scatter;  // the decode kernel writes the new K/V rows (no scatter launch)
+  bool fused_scatter;  // the attention kernels write the new K/V rows (no scatter launch)
+  bool concurrent;     // decode and prefill grids run side by side (decode, prefill, combine)
   void* workspace;
   size_t workspace_bytes;
   DecodeArgs decode;

@@ -27,6 +27,23 @@ struct PrefillArgs {
   int box_keys;      // keys per page box: min(block_size, 128)
   int n_entries;
   int metadata_ready;  // a libcb kernel precedes this one in the step: q and the metadata are visible
+  // The step's new K/V rows (nullptr: none, or already in the cache). With them the
+  // kernel reads a request's own new positions from k_new / v_new instead of the
+  // cache -- each position whose slot_mapping entry is its own slot, which is the
+  // value the cache will hold -- and CTA (request, KV head, tile pair) writes the rows
+  // of its tokens and head into their slots, so the step needs no scatter launch and
+  // nothing in it reads a position written in it.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  // Launched right after the decode kernel of the step (programmatic dependent launch),
+  // while the decode CTAs stream: the kernel needs nothing they write, so it does not
+  // wait for them; the last of its CTAs to finish waits for the decode grid, so that the
+  // completion of this grid implies the decode grid's (the combine launch that follows
+  // reads the decode partials). exit_counter: an int in the workspace header, zero
+  // between steps.
+  int concurrent;
+  int* exit_counter;
   int device_work;     // entries unused: each CTA finds its work in the device metadata (graph
                        // replays: nothing in the arguments depends on the batch); total_ctas is
                        // then an upper bound and the CTAs past the step's work exit at once

@@ -112,6 +112,14 @@ CB_DEV void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       : "memory");
 }
 
+CB_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // An L2 cache policy that marks the lines an access brings in as the first to
 // evict: for data read once (the decode KV stream), so that it does not push out
 // of L2 what is read again soon (the split partials).

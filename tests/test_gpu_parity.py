@@ -231,6 +231,56 @@ def test_decode_step_scatter_skips_negative_and_records_out_of_range_slots():
     compare(spec, out, ref)
 
 
+def test_mixed_step_scatter_skips_negative_and_records_out_of_range_slots():
+    """In a step with prefill rows the tile kernel reads the step's own positions from
+    k_new / v_new where their slot is their own, and from the cache otherwise: a
+    prefill row with slot -1 (or past the pool: recorded, skipped) leaves its cache
+    position as it was, and the rows attending to it see that old value, as the
+    oracle's scatter-then-attend has it. Context lengths off the page boundary make
+    pages that straddle the context end."""
+    spec = workloads.custom([1, 40, 1, 19], [300, 21, 1000, 7], num_q_heads=32, num_kv_heads=8,
+                            seed=27)
+    st = GpuStep(spec)
+    slots = spec.slot_mapping.copy()
+    q0 = int(spec.query_start_loc[1])  # the 40-token chunk
+    slots[q0 + 3] = -1
+    slots[q0 + 17] = spec.num_blocks * spec.block_size + 9
+    slots[int(spec.query_start_loc[3]) + 5] = -1  # inside the 19-token prompt
+    st.md["slot_mapping"] = torch.from_numpy(slots).cuda()
+    h = st.host_inputs()
+    k_before, v_before = st.x["k_cache"].clone(), st.x["v_cache"].clone()
+    out = st.run()
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) & 0x2
+    kept = slots.copy()
+    kept[q0 + 17] = -1
+    for name, before in (("k", k_before), ("v", v_before)):
+        want = oracle_cache_bits(spec, before, st.x[name + "_new"], kept)
+        assert np.array_equal(cache_bits(st.x[name + "_cache"])[2:], want[2:]), name
+    oracle.scatter_kv(h["k_cache"], h["v_cache"], h["k_new"], h["v_new"], kept)
+    ref = oracle.paged_attention(h["q"], h["k_cache"], h["v_cache"], spec.query_start_loc,
+                                 spec.seq_lens, spec.block_table, spec.block_size, spec.scale)
+    compare(spec, out, ref)
+
+
+def test_bf16_steps_launch_no_separate_scatter():
+    """Steps whose rows all run on the tensor-core kernels write their new K/V from
+    those kernels: decode-only, prefill-only and mixed steps launch no scatter kernel."""
+    names = cb.kernel_names()
+    wk = names.index("write_kv")
+    for q_lens, ctx in (([1, 1, 1], [100, 2000, 5]), ([30, 200], [0, 64]),
+                        ([1, 30, 1], [700, 16, 9])):
+        spec = workloads.custom(q_lens, ctx, num_q_heads=32, num_kv_heads=8, seed=len(ctx))
+        st = GpuStep(spec)
+        h = st.host_inputs()
+        before = cb.launch_count(wk)
+        out = st.run()
+        torch.cuda.synchronize()
+        assert cb.launch_count(wk) == before, (q_lens, ctx)
+        assert cb.read_error_word(st.ws) == 0
+        compare(spec, out, oracle_step(spec, h))
+
+
 # ------------------------------------------------------------------ decode kernel coverage
 
 
