@@ -94,6 +94,14 @@ CB_DEV int decode_units(const StepArgs& a, int r, int* seq_out, int* t_out) {
   return units_of(seq, a.sliding_window);
 }
 
+// CTAs a partition of U key blocks uses out of a launch of C: at least
+// kDecodeMinBlocksPerCta blocks each, so that a small step is not split into more
+// segments than its combine can merge quickly.
+CB_DEV int decode_ctas_used(long long U, int C) {
+  const long long want = (U + kDecodeMinBlocksPerCta - 1) / kDecodeMinBlocksPerCta;
+  return (int)(want < C ? want : C);
+}
+
 // CTA that owns global key block u (ranges [b*U/C, (b+1)*U/C)).
 CB_DEV int cta_of(long long u, long long U, int C) {
   return (int)(((u + 1) * (long long)C + U - 1) / U) - 1;
@@ -183,7 +191,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();  // sm.scan is reused by the start search below
     // the launch has a CTA per SM; a step with fewer key blocks uses the first U of
     // them (every CTA of the partition keeps at least one block), the rest have none
-    if (U < C) C = (int)U;
+    C = decode_ctas_used(U, C);
     if (b >= C) return;  // uniform over the CTA; no pipeline started
   }
 
@@ -680,7 +688,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 template <int D, int G>
 __global__ void __launch_bounds__(kCombineMaxThreads)
 decode_combine_kernel(const CombineArgs c) {
-  constexpr int kChunk = 12;  // segments whose loads are in flight together
+  constexpr int kChunk = kCombineSegmentsInFlight;
   __shared__ long long red[32];
   __shared__ long long totals[2];
   const int x = blockIdx.x;
@@ -727,13 +735,17 @@ decode_combine_kernel(const CombineArgs c) {
     const int units = decode_units(a, r, &seq, &t);
     const long long U = totals[0];
     if (units == 0 || U == 0) return;
-    const int C = U < (long long)c.num_ctas ? (int)U : c.num_ctas;
+    const int C = decode_ctas_used(U, c.num_ctas);
     b_first = cta_of(totals[1], U, C);
     nseg = cta_of(totals[1] + units - 1, U, C) - b_first + 1;
     if (nseg < 2) return;  // written directly by its CTA
   }
-  const int f = threadIdx.x;  // float4 f of the slice: outputs 4f .. 4f + 3
-  if (f >= c.kv_per_cta * G * D / 4) return;
+  // thread (part, f): float4 f of the slice (outputs 4f .. 4f + 3) over segment range
+  // `part` of the request's; the partitions' results are merged through shared memory
+  const int F = c.kv_per_cta * G * D / 4;
+  const int nparts = c.parts;
+  const int f = threadIdx.x % F;
+  const int part = threadIdx.x / F;
   const int Hq = c.a.num_q_heads;
   const int qh = kvh0 * G + (4 * f) / D;
   const long long slot0 = (long long)r + b_first;
@@ -742,17 +754,18 @@ decode_combine_kernel(const CombineArgs c) {
   const float2* ml_base = c.part_ml + slot0 * Hq + qh;
   const float4* o_base = reinterpret_cast<const float4*>(c.part_o + slot0 * Hq * D) + o_off;
   const int o_stride = Hq * D / 4;
+  const int s_begin = part * nseg / nparts, s_end = (part + 1) * nseg / nparts;
   // the partials of CTAs that finished early may have left L2: ask for them while
   // the decode grid drains (a hint; the values are read after the wait)
-  for (int i = 0; i < nseg; ++i) {
+  for (int i = s_begin; i < s_end; ++i) {
     if ((4 * f) % D == 0) prefetch_l2(ml_base + i * Hq);
     if (f % 8 == 0) prefetch_l2(o_base + (long long)i * o_stride);
   }
   grid_dependency_wait();  // the partials of the decode grid
   float M = -FLT_MAX, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < nseg; s0 += kChunk) {
-    const int n = min(kChunk, nseg - s0);
+  for (int s0 = s_begin; s0 < s_end; s0 += kChunk) {
+    const int n = min(kChunk, s_end - s0);
     float2 ml[kChunk];
     float4 o[kChunk];
 #pragma unroll
@@ -783,6 +796,27 @@ decode_combine_kernel(const CombineArgs c) {
         acc.z = fmaf(w, o[i].z, acc.z);
         acc.w = fmaf(w, o[i].w, acc.w);
       }
+    }
+  }
+  if (nparts > 1) {
+    extern __shared__ float4 red_acc[];  // [nparts * F], then red_ml
+    float2* red_ml = reinterpret_cast<float2*>(red_acc + nparts * F);
+    red_acc[threadIdx.x] = acc;
+    red_ml[threadIdx.x] = make_float2(M, L);
+    __syncthreads();
+    if (part != 0) return;
+    for (int q = 1; q < nparts; ++q) M = fmaxf(M, red_ml[q * F + f].x);
+    L = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < nparts; ++q) {
+      const float2 ml = red_ml[q * F + f];
+      const float4 o = red_acc[q * F + f];
+      const float w = exp2f(ml.x - M);  // 0 for a partition without segments
+      L = fmaf(w, ml.y, L);
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
     }
   }
   const float inv = 1.f / L;
@@ -858,12 +892,13 @@ cudaError_t launch_d(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorM
 }
 
 template <int D>
-cudaError_t launch_combine_d(const CombineArgs& c, dim3 grid, dim3 block, cudaStream_t s) {
+cudaError_t launch_combine_d(const CombineArgs& c, dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s) {
   switch (c.a.num_q_heads / c.a.num_kv_heads) {
-    case 1: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 1>, grid, block, 0, s, c);
-    case 2: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 2>, grid, block, 0, s, c);
-    case 4: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 4>, grid, block, 0, s, c);
-    case 8: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 8>, grid, block, 0, s, c);
+    case 1: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 1>, grid, block, smem, s, c);
+    case 2: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 2>, grid, block, smem, s, c);
+    case 4: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 4>, grid, block, smem, s, c);
+    case 8: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 8>, grid, block, smem, s, c);
   }
   return cudaErrorInvalidValue;
 }
@@ -878,9 +913,12 @@ cudaError_t launch_decode_combine(const CombineArgs& c, cudaStream_t stream) {
   if (c.kv_per_cta <= 0 || c.a.num_kv_heads % c.kv_per_cta != 0 || f4 > kCombineMaxThreads)
     return cudaErrorInvalidValue;
   const dim3 grid(nx, c.a.num_kv_heads / c.kv_per_cta);
-  const dim3 block((f4 + 31) / 32 * 32);
-  if (c.a.head_dim == 64) return launch_combine_d<64>(c, grid, block, stream);
-  return launch_combine_d<128>(c, grid, block, stream);
+  if (c.parts < 1 || f4 * c.parts > kCombineMaxThreads) return cudaErrorInvalidValue;
+  // f4 = kv_per_cta x G x D / 4 is a multiple of 32
+  const dim3 block(f4 * c.parts);
+  const size_t smem = c.parts > 1 ? (size_t)block.x * (sizeof(float4) + sizeof(float2)) : 0;
+  if (c.a.head_dim == 64) return launch_combine_d<64>(c, grid, block, smem, stream);
+  return launch_combine_d<128>(c, grid, block, smem, stream);
 }
 
 size_t decode_smem_bytes(int stages, int stage_bytes, int q_slot_bytes) {

@@ -11,6 +11,7 @@ constexpr int kDecodeMaxStages = 8;
 constexpr int kDecodeMaxHeads = 8;          // KV heads per CTA (one consumer warp each)
 constexpr int kDecodeSmemLimit = 232448;    // 227 KiB dynamic shared memory per CTA
 constexpr int kDecodeTableCtas = 256;       // CTAs whose start is passed in the arguments
+constexpr int kDecodeMinBlocksPerCta = 4;   // key blocks per CTA at least (small steps)
 constexpr int CB_DEVERR_BLOCK_ID_CODE = 0x1;
 constexpr int CB_DEVERR_SLOT_CODE = 0x2;
 constexpr int CB_DEVERR_TIMEOUT_CODE = 0x4;
@@ -66,7 +67,8 @@ struct CombineEntry {
 };
 
 constexpr int kCombineListMax = 256;    // split requests the host lists in the arguments
-constexpr int kCombineMaxThreads = 512;  // one per four outputs of a CTA's KV heads
+constexpr int kCombineMaxThreads = 512;  // per CTA: four outputs of its KV heads each, x parts
+constexpr int kCombineSegmentsInFlight = 12;  // partials a combine thread loads at once
 
 struct CombineArgs {
   StepArgs a;
@@ -74,6 +76,7 @@ struct CombineArgs {
   const float* part_o;    // the decode launch's partials
   const float2* part_ml;
   int kv_per_cta;         // KV heads merged by one CTA (divides num_kv_heads; x G x D / 4 <= 512)
+  int parts;              // threads per output (each merges a share of the segments; >= 1)
   int n_entries;  // >= 0: entries[0 .. n_entries) are the split requests; -1: the
                   // kernel finds them from the device metadata (one CTA per request)
   CombineEntry entries[kCombineListMax];

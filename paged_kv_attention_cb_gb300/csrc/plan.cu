@@ -246,7 +246,9 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
       const long long bytes = U * 16LL * 2 * a.num_kv_heads * a.head_dim * 2;
       C = sm_count() - prefill_sm_share(bytes, flops, prefill_total_ctas, sm_count());
     }
-    d.num_ctas = (int)std::min<long long>(C, U);
+    // at least kDecodeMinBlocksPerCta key blocks per CTA: a small step split over every
+    // SM spends more on merging its many segments than it gains in streaming
+    d.num_ctas = (int)std::min<long long>(C, (U + kDecodeMinBlocksPerCta - 1) / kDecodeMinBlocksPerCta);
     d.units_on_device = 0;
     // each decode row's new K/V is written by the CTA that reads the request's last key
     // block (the decode kernel is then the step's first)
@@ -302,6 +304,12 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
       c.entries[c.n_entries++] = CombineEntry{r, h_qsl[r], b0, b1 - b0 + 1};
     }
     c.kv_per_cta = combine_kv_per_cta(a, c.n_entries >= 0 ? c.n_entries : a.num_requests);
+    // a request split into many segments is merged by several threads per output, each
+    // over a share of the segments (fewer dependent rounds of loads)
+    int max_seg = 0;
+    for (int e = 0; e < c.n_entries; ++e) max_seg = std::max(max_seg, c.entries[e].nseg);
+    const int f4 = c.kv_per_cta * G * a.head_dim / 4;
+    c.parts = max_seg > 2 * kCombineSegmentsInFlight ? std::max(1, kCombineMaxThreads / f4) : 1;
     plan.has_combine = c.n_entries != 0;
   }
 }
@@ -350,6 +358,7 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   combine_common(plan.combine, a, d);
   plan.combine.n_entries = -1;  // the batch's split requests are found on the device
   plan.combine.kv_per_cta = combine_kv_per_cta(a, a.num_requests);
+  plan.combine.parts = 1;
   plan.has_combine = with_decode;
 
   PrefillArgs& pa = plan.prefill[0];
