@@ -281,6 +281,25 @@ def test_bf16_steps_launch_no_separate_scatter():
         compare(spec, out, oracle_step(spec, h))
 
 
+@pytest.mark.parametrize("case", ["long_context_chunks", "window", "g1_d64", "g16"])
+def test_prefill_long_context_chunks(case):
+    """Chunks over long contexts, each (tile pair, KV head) CTA walking many key tiles,
+    with windows, G 1 with head_dim 64, and G 16."""
+    if case == "long_context_chunks":
+        spec = workloads.custom([100, 300, 1], [20000, 5000, 700], num_q_heads=32,
+                                num_kv_heads=8, seed=41)
+    elif case == "window":
+        spec = workloads.custom([200, 64], [12000, 3000], num_q_heads=32, num_kv_heads=8,
+                                seed=42, sliding_window=2500)
+    elif case == "g1_d64":
+        spec = workloads.custom([150, 40], [9000, 16000], num_q_heads=4, num_kv_heads=4,
+                                head_dim=64, seed=43)
+    else:
+        spec = workloads.custom([90, 33], [7000, 4000], num_q_heads=32, num_kv_heads=2,
+                                seed=44)
+    full_check(spec)
+
+
 # ------------------------------------------------------------------ decode kernel coverage
 
 
