@@ -75,7 +75,7 @@ __host__ __device__ constexpr int tile_bytes() {
 }
 
 struct PfBars {
-  uint64_t q_full;              // both tiles' query rows in shared memory (eight warps)
+  uint64_t q_full;              // both tiles' query rows in shared memory (tensor copies)
   uint64_t full[kMaxStages];    // ring slot loaded (K0, V0, K1, V1, ...)
   uint64_t empty[kMaxStages];   // ring slot released by the MMAs that read it
   uint64_t s_full[kTiles];      // S_t in TMEM (and the PV product before it complete)
@@ -131,6 +131,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __grid_constant__ CUtensorMap tmap_kn,
                     const __grid_constant__ CUtensorMap tmap_vn,
+                    const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ PrefillArgs p) {
   static_assert(D == 64 || D == 128, "head_dim");
   constexpr int kHalves = D / 64;
@@ -212,7 +213,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const bool has_b = qt0 + 1 < nq;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.q_full, kSoftmaxThreads / 32);
+    mbar_init(&bar.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar.full[s], 1);
       mbar_init(&bar.empty[s], 1);
@@ -229,6 +230,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     fence_barrier_init();
   }
   if (warp == kWarpTma && lane == 0) {
+    prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_k);
     if (p.k_new != nullptr) prefetch_tensormap(&tmap_kn);
   }
@@ -296,6 +298,18 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         sl[q4] = (pos >= ctx && pos < seq) ? __ldg(p.slot_mapping + q_start + (pos - ctx)) : -1;
       }
     };
+    // the two query tiles: box (64 of D, the G heads of KV head g, TQ tokens) per tile and
+    // half of D lands as the tile's 128 rows (token-major, head-minor) in the 128B-swizzled
+    // K-major layout the products read; tokens past the request are never output rows
+    // (past T they read as zeros)
+    if (!is_v && lane == 0) {
+      const int G = p.a.num_q_heads / Hkv;
+      mbar_arrive_expect_tx(&bar.q_full, (uint32_t)((has_b ? 2 : 1) * kTile));
+      for (int t = 0; t < (has_b ? 2 : 1); ++t)
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_3d(sQ + t * kTile + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G,
+                      q_start + (qt0 + t) * p.tile_tokens);
+    }
     if (p.metadata_ready && !p.concurrent) grid_dependency_wait();  // the step's scatter launch
     int ids_cur = tile_pages(0);
     long long sl_cur[4], sl_next[4];
@@ -520,7 +534,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
       const int Hkv = p.a.num_kv_heads;
       const int n = (cta_tok_end - cta_tok0) * kPerTok;
-      constexpr int kBatch = 4;
+      // 16 rows' chunks in flight per lane: the copy is latency-bound, and a CTA whose
+      // key range is short must not outlast its attention work because of it
+      constexpr int kBatch = 16;
       for (int e0 = 0; e0 < n; e0 += 32 * kBatch) {
         uint4 v[kBatch];
         long long sl[kBatch];
@@ -562,22 +578,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok = tok0 + row / G;
     const int hh = row % G;
     const bool row_valid = tile_live && tok < q_len;
-    // this row's query (one token, one head: head_dim contiguous bf16) into the
-    // swizzled K-major tile: 16-byte chunk c of row `row` goes to chunk c ^ (row % 8)
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.a.q) +
-                                                        ((long long)(q_start + tok) * p.a.num_q_heads + g * G + hh) * D);
-      uint8_t* dst = sQ + t * kTile + row * 128;
-      uint4 x[D / 8];
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) x[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        *reinterpret_cast<uint4*>(dst + (c >> 3) * kHalfBytes + (((c & 7) ^ (row & 7)) << 4)) = x[c];
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar.q_full);
-    }
     if (tile_live) {
       const int qpos = ctx + tok;
       const int max_kv = min(qpos, seq - 1);
@@ -729,6 +729,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // consumed, so only the latest copy of each slot can be in flight: waiting for its
   // phase drains the ring before the CTA's shared memory is released.
   if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&bar.abort)) {
+    mbar_wait(&bar.q_full, 0);  // the query tiles' copies
     for (int s2 = 0; s2 < kStages; ++s2) {
       const int i = bar.issued[s2];
       if (i >= 0) mbar_wait(&bar.full[s2], (uint32_t)((i / kStages) & 1));
@@ -799,6 +800,17 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
     if (err == cudaSuccess) err = encode(&mvn, const_cast<void*>(p.v_new), 3, nd, ns, nb);
     if (err != cudaSuccess) return err;
   }
+  // q [T, Hq, D] as (d, head, token); box: 64 of d, the G heads of a KV head, the
+  // tokens of a 128-row tile
+  CUtensorMap mq;
+  {
+    const int G = a.num_q_heads / a.num_kv_heads;
+    cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
+    cuuint64_t qs[2] = {(cuuint64_t)D * e, (cuuint64_t)a.num_q_heads * D * e};
+    cuuint32_t qb[3] = {64, (cuuint32_t)G, (cuuint32_t)p.tile_tokens};
+    err = encode(&mq, const_cast<void*>(a.q), 3, qd, qs, qb);
+    if (err != cudaSuccess) return err;
+  }
   auto kern = prefill_tile_kernel<D>;
   static bool attr_set = false;
   constexpr size_t smem = smem_bytes<D>();
@@ -808,7 +820,7 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
     attr_set = true;
   }
   return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mk, mv, mkn,
-                    mvn, p);
+                    mvn, mq, p);
 }
 
 }  // namespace
