@@ -58,8 +58,7 @@ constexpr int kSoftmaxThreads = kTiles * kRows;
 constexpr int kWarpTma = kSoftmaxThreads / 32;
 constexpr int kWarpMma = kWarpTma + 1;
 constexpr int kWarpTmaV = kWarpMma + 1;  // kWarpTma loads K tiles, kWarpTmaV V tiles
-constexpr int kWarpScatter = kWarpTmaV + 1;  // writes the CTA's new K/V rows to the cache
-constexpr int kThreads = kSoftmaxThreads + 128;
+constexpr int kThreads = kSoftmaxThreads + 96;
 // Register bound: up to three warps share each SM sub-partition's 16K registers,
 // so a thread may hold at most 168; a 384-thread launch bound makes the compiler keep to it.
 constexpr int kThreadsBound = 384;
@@ -521,52 +520,6 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // commit tracks them all; it completes whether or not the loop ran to its end)
     umma_commit_elect(&bar.drain);
     mbar_wait_warp(&bar.drain, 0);
-  } else if (warp == kWarpScatter) {
-    // =================================================== scatter warp
-    // The new K and V rows of this CTA's tokens for KV head g go to their slots
-    // (a slot below zero is skipped, one past the pool recorded and skipped). The
-    // tile pairs of all KV heads cover every (token, head) of the request once.
-    // Nothing in the step reads these positions from the cache (the TMA warps read
-    // them from k_new), so the writes need no ordering with the rest of the CTA.
-    if (p.k_new != nullptr) {
-      constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
-      constexpr int kPerTok = 2 * kRowChunks;
-      const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
-      const int Hkv = p.a.num_kv_heads;
-      const int n = (cta_tok_end - cta_tok0) * kPerTok;
-      // 16 rows' chunks in flight per lane: the copy is latency-bound, and a CTA whose
-      // key range is short must not outlast its attention work because of it
-      constexpr int kBatch = 16;
-      for (int e0 = 0; e0 < n; e0 += 32 * kBatch) {
-        uint4 v[kBatch];
-        long long sl[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = e0 + lane + 32 * u;
-          sl[u] = -1;
-          if (e < n) {
-            const int tok = q_start + cta_tok0 + e / kPerTok;
-            const int rem = e % kPerTok;
-            const uint4* src = static_cast<const uint4*>(rem < kRowChunks ? p.k_new : p.v_new);
-            sl[u] = __ldg(p.slot_mapping + tok);
-            v[u] = __ldg(src + ((long long)tok * Hkv + g) * kRowChunks + rem % kRowChunks);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = e0 + lane + 32 * u;
-          if (e < n && sl[u] >= 0) {
-            const int rem = e % kPerTok;
-            if (sl[u] < num_slots) {
-              uint4* dstc = static_cast<uint4*>(rem < kRowChunks ? p.a.k_cache : p.a.v_cache);
-              dstc[(sl[u] * Hkv + g) * kRowChunks + rem % kRowChunks] = v[u];
-            } else if (rem == 0) {
-              record_error(p.a.error_word, 0x2);
-            }
-          }
-        }
-      }
-    }
   } else {
     // =================================================== softmax warpgroups
     const int t = warp >> 2;             // query tile of this group
@@ -713,6 +666,50 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       } else if (lane == 0) {
         record_error(p.a.error_word, 0x4);
         set_abort(&bar.abort);
+      }
+      // ---- the new K and V rows of this CTA's tokens for KV head g to their slots (a slot
+      // below zero is skipped, one past the pool recorded and skipped), after the CTA's
+      // attention work so that the copy does not compete with it. The tile pairs of all
+      // KV heads cover every (token, head) of the request once; nothing in the step reads
+      // these positions from the cache (the TMA warps read them from k_new).
+      if (p.k_new != nullptr) {
+        constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
+        constexpr int kPerTok = 2 * kRowChunks;
+        const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
+        const int Hkv = p.a.num_kv_heads;
+        const int nthr = has_b ? kSoftmaxThreads : kRows;
+        const int me = t * kRows + row;
+        const int n = (cta_tok_end - cta_tok0) * kPerTok;
+        constexpr int kBatch = 8;
+        for (int e0 = 0; e0 < n; e0 += nthr * kBatch) {
+          uint4 v[kBatch];
+          long long sl[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + me + nthr * u;
+            sl[u] = -1;
+            if (e < n) {
+              const long long tok = q_start + cta_tok0 + e / kPerTok;
+              const int rem = e % kPerTok;
+              const uint4* src = static_cast<const uint4*>(rem < kRowChunks ? p.k_new : p.v_new);
+              sl[u] = __ldg(p.slot_mapping + tok);
+              v[u] = __ldg(src + (tok * Hkv + g) * kRowChunks + rem % kRowChunks);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + me + nthr * u;
+            if (e < n && sl[u] >= 0) {
+              const int rem = e % kPerTok;
+              if (sl[u] < num_slots) {
+                uint4* dstc = static_cast<uint4*>(rem < kRowChunks ? p.a.k_cache : p.a.v_cache);
+                dstc[(sl[u] * Hkv + g) * kRowChunks + rem % kRowChunks] = v[u];
+              } else if (rem == 0) {
+                record_error(p.a.error_word, 0x2);
+              }
+            }
+          }
+        }
       }
     }
   }
