@@ -5,23 +5,30 @@
 // request's query tile: context_len = seq_len - q_len, query token local_q
 // attends kv_pos 0 .. context_len + local_q (or the last sliding_window of
 // them), each resolved through block_table[req][kv_pos / BLOCK_SIZE]. The
-// chunk's own tokens were scattered into the cache before this kernel runs
-// (section "Extension: combining with chunked prefill": a chunk with a context
-// continues a prompt already in the cache). Prefill is compute-bound
+// chunk's own tokens are this step's new K/V rows (section "Extension: combining
+// with chunked prefill": a chunk with a context continues a prompt already in the
+// cache). Prefill is compute-bound
 // ("Continuous batching mechanics", d9bl.com), so both products are dense
 // contractions on the 5th-generation tensor cores:
 //
 // * Tiles. A query tile is 128 rows = 128/G tokens x the G query heads of one
-//   KV head (grouped-query packing: each K/V tile serves all G heads). One CTA
-//   owns two consecutive query tiles A and B of a request and walks the union
-//   of their key ranges in tiles of 128 keys, so each K/V tile loaded serves
-//   256 rows. Only the tiles at a bound need the per-row causal or window check.
-// * Staging. The softmax threads copy their query rows into shared memory in
-//   the 128B-swizzled K-major layout the tensor cores read. Two TMA warps load
-//   the K and the V tiles page by page (a 4-D box per page and 64-wide half of
-//   head_dim through the block table, 128B swizzle, one lane per box) into one
-//   mbarrier ring in the order K0, V0, K1, V1, ...; pages past the request read
-//   as zeros.
+//   KV head (grouped-query packing: each K/V tile serves all G heads). A unit of
+//   work is two consecutive query tiles A and B of a request for one KV head; its
+//   key range (the union of the two tiles') is walked in tiles of 128 keys, so
+//   each K/V tile loaded serves 256 rows. Only the tiles at a bound need the
+//   per-row causal or window check.
+// * Persistent CTAs. One CTA per SM (at most one per unit) claims units from the
+//   step's list, heaviest first, through an atomic counter in the workspace, and
+//   passes each to its roles through a two-slot ring in shared memory; the next
+//   unit's query tiles and first K/V tiles load while the current one finishes.
+// * Staging. The K TMA warp loads each unit's two query tiles (a 3-D box of the
+//   G heads x TQ tokens per half of head_dim). Two TMA warps load the K and the V
+//   tiles page by page (a 4-D box per page and 64-wide half of head_dim through
+//   the block table, 128B swizzle, one lane per box) into one mbarrier ring in
+//   the order K0, V0, K1, V1, ...; pages past the request read as zeros. The
+//   step's own new positions are read from k_new / v_new where their slot is
+//   their own; the softmax warps of CTAs with no unit left copy the new rows into
+//   the cache.
 // * Contraction. One MMA warp issues, for key tile j,
 //     O_A += P_A V_j,  S_A = Q_A K_{j+1}^T,  O_B += P_B V_j,  S_B = Q_B K_{j+1}^T
 //   (M 128; N head_dim or 128; K in steps of 16), accumulating in TMEM, whose
@@ -58,10 +65,20 @@ constexpr int kSoftmaxThreads = kTiles * kRows;
 constexpr int kWarpTma = kSoftmaxThreads / 32;
 constexpr int kWarpMma = kWarpTma + 1;
 constexpr int kWarpTmaV = kWarpMma + 1;  // kWarpTma loads K tiles, kWarpTmaV V tiles
-constexpr int kThreads = kSoftmaxThreads + 96;
-// Register bound: up to three warps share each SM sub-partition's 16K registers,
-// so a thread may hold at most 168; a 384-thread launch bound makes the compiler keep to it.
-constexpr int kThreadsBound = 384;
+// The fourth warp of the last warpgroup (warp 11) has no role: setmaxnreg is executed per
+// warpgroup, so the group of the TMA and MMA warps is complete.
+constexpr int kThreads = kSoftmaxThreads + 128;
+// Registers: 384 threads launch with 168 each (64,512 of the SM's 65,536); a thread's S
+// row alone is 128 of them. The TMA and MMA warpgroup then gives back registers down to
+// kRegsIssue each and the softmax warpgroups take kRegsSoftmax each. The roles share no
+// code after the split, so the compiler allocates each within its own budget (with one
+// budget for the whole kernel the softmax loop spilled).
+constexpr int kThreadsBound = kThreads;
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsIssue = 152;
+constexpr int kRegsSoftmax = 176;
+static_assert(kRegsIssue * 128 + kRegsSoftmax * kSoftmaxThreads <= kRegsLaunch * kThreads,
+              "an increase waits for registers the launch does not hold");
 constexpr float kRescaleLog2 = 8.f;    // raise the running max only when it grows by > 2^8
 constexpr uint32_t kTmemCols = 512;    // S_A 0-127, S_B 128-255, O_A, O_B from 256 (head_dim each)
 constexpr int kHalfBytes = kRows * 128;  // 128 rows x 64 bf16: one swizzle-atom column of a tile
@@ -73,27 +90,71 @@ __host__ __device__ constexpr int tile_bytes() {
   return (D / 64) * kHalfBytes;
 }
 
+// A unit of work: query tiles 2 pair and 2 pair + 1 of request r, KV head g (live = 0:
+// no more units).
+struct UnitDesc {
+  int r, q_start, q_len, seq_len, g, pair, live;
+};
+
+// Geometry of a unit (request, KV head g, pair of query tiles): the union of the two
+// tiles' key ranges is walked in key tiles kt0 .. kt0 + nkt - 1.
+struct Geo {
+  int r, g, q_start, q_len, seq, ctx, qt0, has_b, tok0, tok_end, kt0, nkt;
+};
+
+CB_DEV Geo geo_of(int r, int q_start, int q_len, int seq_len, int g, int pair, int TQ, int W) {
+  Geo e;
+  e.r = r;
+  e.g = g;
+  e.q_start = q_start;
+  e.q_len = q_len;
+  e.seq = seq_len;
+  e.ctx = seq_len - q_len;
+  e.qt0 = kTiles * pair;
+  e.has_b = e.qt0 + 1 < (q_len + TQ - 1) / TQ;
+  e.tok0 = e.qt0 * TQ;
+  e.tok_end = min(q_len, e.tok0 + kTiles * TQ);
+  const int first_key = W > 0 ? max(0, e.ctx + e.tok0 - W + 1) : 0;
+  const int last_key = min(e.ctx + e.tok_end - 1, e.seq - 1);
+  e.kt0 = first_key / kKeys;
+  e.nkt = last_key / kKeys - e.kt0 + 1;
+  return e;
+}
+
+CB_DEV Geo geo_of(const UnitDesc& d, int TQ, int W) {
+  return geo_of(d.r, d.q_start, d.q_len, d.seq_len, d.g, d.pair, TQ, W);
+}
+
+// Warps that read the unit ring (the V TMA warp, the MMA warp, eight softmax warps).
+constexpr int kUnitReaders = 2 + kSoftmaxThreads / 32;
+
 struct PfBars {
   uint64_t q_full;              // both tiles' query rows in shared memory (tensor copies)
+  uint64_t q_empty;             // the unit's last S products are done (query buffer free)
   uint64_t full[kMaxStages];    // ring slot loaded (K0, V0, K1, V1, ...)
   uint64_t empty[kMaxStages];   // ring slot released by the MMAs that read it
   uint64_t s_full[kTiles];      // S_t in TMEM (and the PV product before it complete)
   uint64_t p_full[kTiles];      // P_t in TMEM (the group's four warps)
   uint64_t o_done[kTiles];      // O_t final (its last PV product complete)
+  uint64_t o_free[kTiles];      // O_t read by the epilogue (the group's four warps)
+  uint64_t unit_full[2];        // unit ring slot written (the scheduler)
+  uint64_t unit_empty[2];       // unit ring slot read (every other warp)
+  UnitDesc unit[2];
   uint64_t drain;
   uint64_t never;               // nothing arrives here: the test hook's wait on it runs out
   uint32_t tmem_base;
   int abort;                    // a wait gave up: the other roles stop waiting
   int issued[kMaxStages];       // ring index of the latest copy issued into each slot
+  int q_loads;                  // query-tile copies issued so far
 };
 
 // Ring depth: the shared memory left after the two query tiles, the barriers
 // and the alignment slack, at most kMaxStages tiles.
 template <int D>
 __host__ __device__ constexpr int ring_stages() {
-  return (kPrefillSmemLimit - 1024 - 256 - kTiles * tile_bytes<D>()) / tile_bytes<D>() > kMaxStages
+  return (kPrefillSmemLimit - 1024 - (int)sizeof(PfBars) - kTiles * tile_bytes<D>()) / tile_bytes<D>() > kMaxStages
              ? kMaxStages
-             : (kPrefillSmemLimit - 1024 - 256 - kTiles * tile_bytes<D>()) / tile_bytes<D>();
+             : (kPrefillSmemLimit - 1024 - (int)sizeof(PfBars) - kTiles * tile_bytes<D>()) / tile_bytes<D>();
 }
 
 template <int D>
@@ -147,14 +208,17 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  Work w;
-  PrefillEntry ent;
+  const int Hkv = p.a.num_kv_heads;
+  const int G = p.a.num_q_heads / Hkv;
+  const int TQ = p.tile_tokens;
+  const int W = p.a.sliding_window;
+  // Graph replays: the one unit of this CTA, found with a block scan over the device
+  // metadata (request order; each request with q_len > 1 has ceil(n_qtiles / 2) * Hkv).
+  __shared__ UnitDesc s_first;  // the unit found on the device (kept out of registers)
   if (p.device_work) {
-    // request order; every request with q_len > 1 gets ceil(n_qtiles / 2) * Hkv CTAs
     grid_dependency_wait();
     __shared__ int s_tot[kThreads / 32];
     __shared__ int s_hit[2];
-    const int Hkv = p.a.num_kv_heads;
     if (threadIdx.x == 0) s_hit[0] = -1;
     int carry = 0;
     for (int base_r = 0; base_r < p.a.num_requests; base_r += kThreads) {
@@ -162,7 +226,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       int n = 0;
       if (rr < p.a.num_requests) {
         const int ql = __ldg(p.a.query_start_loc + rr + 1) - __ldg(p.a.query_start_loc + rr);
-        if (ql > 1) n = ((ql + p.tile_tokens - 1) / p.tile_tokens + 1) / 2 * Hkv;
+        if (ql > 1) n = ((ql + TQ - 1) / TQ + 1) / 2 * Hkv;
       }
       int v = n;  // inclusive warp scan
 #pragma unroll
@@ -186,33 +250,16 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (s_hit[0] < 0) return;  // past the step's work: uniform over the CTA
     const int rr = s_hit[0];
     const int k = s_hit[1];
-    ent.r = rr;
-    ent.q_start = __ldg(p.a.query_start_loc + rr);
-    ent.q_len = __ldg(p.a.query_start_loc + rr + 1) - ent.q_start;
-    ent.seq_len = __ldg(p.a.seq_lens + rr);
-    ent.n_qtiles = (ent.q_len + p.tile_tokens - 1) / p.tile_tokens;
-    const int npairs = (ent.n_qtiles + 1) / 2;
-    w = Work{0, k % Hkv, npairs - 1 - k / Hkv};
-  } else {
-    w = work_of(p, blockIdx.x);
-    if (w.e < 0) return;  // uniform over the CTA, before any barrier
-    ent = p.entries[w.e];
+    const int qs0 = __ldg(p.a.query_start_loc + rr);
+    const int ql = __ldg(p.a.query_start_loc + rr + 1) - qs0;
+    const int npairs = ((ql + TQ - 1) / TQ + 1) / 2;
+    if (threadIdx.x == 0)
+      s_first = UnitDesc{rr, qs0, ql, __ldg(p.a.seq_lens + rr), k % Hkv, npairs - 1 - k / Hkv, 1};
   }
-
-  // ---- request geometry
-  const int r = ent.r;
-  const int g = w.g;
-  const int q_start = ent.q_start;
-  const int q_len = ent.q_len;
-  const int seq = ent.seq_len;
-  const int ctx = seq - q_len;
-  const int TQ = p.tile_tokens;
-  const int nq = (q_len + TQ - 1) / TQ;
-  const int qt0 = kTiles * w.pair;
-  const bool has_b = qt0 + 1 < nq;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar.full[s], 1);
       mbar_init(&bar.empty[s], 1);
@@ -220,11 +267,17 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bar.s_full[t], 1);
       mbar_init(&bar.p_full[t], 4);
+      mbar_init(&bar.o_done[t], 1);
+      mbar_init(&bar.o_free[t], 4);
     }
-    for (int t = 0; t < kTiles; ++t) mbar_init(&bar.o_done[t], 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&bar.unit_full[u], 1);
+      mbar_init(&bar.unit_empty[u], kUnitReaders);
+    }
     mbar_init(&bar.drain, 1);
     mbar_init(&bar.never, 1);
     bar.abort = 0;
+    bar.q_loads = 0;
     for (int s = 0; s < kStages; ++s) bar.issued[s] = -1;
     fence_barrier_init();
   }
@@ -248,22 +301,67 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
   tcgen05_fence_after();
   allow_dependent_launch();
   const uint32_t tmem = bar.tmem_base;
-
-  // the CTA walks the union of its two tiles' key ranges
-  const int cta_tok0 = qt0 * TQ;
-  const int cta_tok_end = min(q_len, cta_tok0 + kTiles * TQ);
-  const int W = p.a.sliding_window;
-  const int first_key = W > 0 ? max(0, ctx + cta_tok0 - W + 1) : 0;
-  const int last_key = min(ctx + cta_tok_end - 1, seq - 1);
-  const int kt0 = first_key / kKeys;
-  const int nkt = last_key / kKeys - kt0 + 1;
   bool ok = true;
 
+  // ---- teardown, run by every warp at the end of its role (each role ends in its own
+  // copy, so that the roles' code shares no join point: their register budgets differ)
+  auto teardown = [&]() {
+    tcgen05_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+      tcgen05_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    // If a wait gave up, copies may be in flight that no MMA consumed. The ring's slots
+    // are filled in index order and a slot is refilled only after its previous copy was
+    // consumed, so only the latest copy of each slot can be in flight: waiting for its
+    // phase drains the ring before the CTA's shared memory is released (and likewise the
+    // latest query tiles' copy).
+    if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&bar.abort)) {
+      if (bar.q_loads > 0) mbar_wait(&bar.q_full, (uint32_t)((bar.q_loads - 1) & 1));
+      for (int s2 = 0; s2 < kStages; ++s2) {
+        const int i = bar.issued[s2];
+        if (i >= 0) mbar_wait(&bar.full[s2], (uint32_t)((i / kStages) & 1));
+      }
+    }
+    // The last CTA to finish sets the claim counters and the exit counter back to zero for
+    // the next step; launched beside the decode kernel, it also waits for the decode grid,
+    // so that this grid completes only after it (the combine launch that follows waits for
+    // this grid and reads the decode partials).
+    if (threadIdx.x == 0 && !p.device_work) {
+      if (atomicAdd(p.exit_counter, 1) == (int)gridDim.x - 1) {
+        atomicExch(p.exit_counter, 0);
+        atomicExch(p.unit_counter, 0);
+        atomicExch(p.scatter_counter, 0);
+        if (p.concurrent) grid_dependency_wait();
+      }
+    }
+  };
+
+  // Every role reads the CTA's units in the same order from a two-slot ring that the K
+  // TMA warp fills: with the work found on the device, the CTA's one unit; otherwise the
+  // next unit of the step's list (heaviest first) claimed through an atomic counter, so
+  // that a CTA takes a new unit as soon as it can (and CTAs that start late, on SMs a
+  // decode grid held, take what is left).
+  auto read_unit = [&](int u, UnitDesc& d) -> bool {
+    if (!mbar_wait_warp_or_abort(&bar.unit_full[u & 1], (uint32_t)((u >> 1) & 1), &bar.abort))
+      return false;
+    d = bar.unit[u & 1];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.unit_empty[u & 1]);
+    return true;
+  };
+
+  if (warp >= kWarpTma) {
+  // The issuing warpgroup caps its registers (each role branch below ends in its own
+  // teardown, so no code after this point is shared with the softmax warps).
+  setmaxnreg_dec<kRegsIssue>();
   if (warp == kWarpTma || warp == kWarpTmaV) {
     // =================================================== TMA warps
     // One warp loads the K tiles (ring indices 2j), the other the V tiles (2j + 1):
     // a 16-key page makes 16 boxes per tile, and one warp issuing them all would
-    // fall behind the tensor pipe.
+    // fall behind the tensor pipe. The K warp also schedules the units and loads their
+    // query tiles.
     const int is_v = warp == kWarpTmaV;
     const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
     const CUtensorMap* nmap = is_v ? &tmap_vn : &tmap_kn;
@@ -271,178 +369,229 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint4* cache = static_cast<const uint4*>(is_v ? p.a.v_cache : p.a.k_cache);
     const bool fuse = p.k_new != nullptr;
     const int BS = p.a.block_size;
-    const int Hkv = p.a.num_kv_heads;
     const int box = p.box_keys;
     const int lg_box = __ffs(box) - 1;  // box and block_size are powers of two
     const int lg_bs = __ffs(BS) - 1;
     const int bs_mask = BS - 1;
     const int ppt = kKeys / box;  // pages per key tile
     const int nbox = ppt * kHalves;
-    const int npages_req = (seq + BS - 1) / BS;
-    const int32_t* bt = p.a.block_table + (long long)r * p.a.bt_stride;
-    // page ids of key tile j (lane i < ppt: page i of the tile); checked where
-    // they are used, so that the load of the next tile's ids does not stall
-    auto tile_pages = [&](int j) -> int {
-      const int lp = (((kt0 + j) * kKeys) >> lg_bs) + lane;
-      return (lane < ppt && lp < npages_req) ? __ldg(bt + bt_entry(lp, p.a.ring_blocks)) : 0;
-    };
-    // slot_mapping entries of tile j's keys lane + 32 q that are this step's new
-    // positions (ctx <= pos < seq); -1 elsewhere
-    auto tile_slots = [&](int j, long long (&sl)[4]) {
-      const int key_base = (kt0 + j) * kKeys;
-      if (!(fuse && key_base + kKeys > ctx && key_base < seq)) return;  // no new position
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int pos = key_base + lane + 32 * q4;
-        sl[q4] = (pos >= ctx && pos < seq) ? __ldg(p.slot_mapping + q_start + (pos - ctx)) : -1;
-      }
-    };
-    // the two query tiles: box (64 of D, the G heads of KV head g, TQ tokens) per tile and
-    // half of D lands as the tile's 128 rows (token-major, head-minor) in the 128B-swizzled
-    // K-major layout the products read; tokens past the request are never output rows
-    // (past T they read as zeros)
-    if (!is_v && lane == 0) {
-      const int G = p.a.num_q_heads / Hkv;
-      mbar_arrive_expect_tx(&bar.q_full, (uint32_t)((has_b ? 2 : 1) * kTile));
-      for (int t = 0; t < (has_b ? 2 : 1); ++t)
-        for (int h = 0; h < kHalves; ++h)
-          tma_load_3d(sQ + t * kTile + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G,
-                      q_start + (qt0 + t) * p.tile_tokens);
-    }
     if (p.metadata_ready && !p.concurrent) grid_dependency_wait();  // the step's scatter launch
-    int ids_cur = tile_pages(0);
-    long long sl_cur[4], sl_next[4];
-    tile_slots(0, sl_cur);
-    for (int j = 0; j < nkt; ++j) {
-      const int i = 2 * j + is_v;
-      const int s = i % kStages;
-      uint8_t* dst = sRing + s * kTile;
-      const int key_base = (kt0 + j) * kKeys;
-      // the next tile's page ids and slots are read while this one waits for its slot
-      const int ids_next = j + 1 < nkt ? tile_pages(j + 1) : 0;
-      if (j + 1 < nkt) tile_slots(j + 1, sl_next);
-      if (i >= kStages &&
-          !mbar_wait_warp_or_abort(&bar.empty[s], (uint32_t)(((i / kStages) - 1) & 1), &bar.abort)) {
+    int i_base = 0;  // ring index of this unit's K_0
+    for (int u = 0; ok; ++u) {
+      UnitDesc d;
+      if (!is_v) {
+        // ---- scheduler (the ring slot is free once every reader is done with unit u - 2)
+        if (u >= 2 && !mbar_wait_warp_or_abort(&bar.unit_empty[u & 1], (uint32_t)(((u >> 1) - 1) & 1),
+                                               &bar.abort)) {
+          ok = false;
+          break;
+        }
+        if (p.device_work) {
+          d = u == 0 ? s_first : UnitDesc{-1, 0, 0, 0, 0, 0, 0};
+        } else {
+          // claimed once the previous unit's loads are all issued (the ring's depth
+          // ahead of its products), so that a unit goes to the first CTA that can
+          // start it: claimed earlier, a light unit could wait behind a heavy one
+          int idx = 0;
+          if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
+          idx = __shfl_sync(0xffffffffu, idx, 0);
+          d = UnitDesc{-1, 0, 0, 0, 0, 0, 0};
+          if (idx < p.total_units) {
+            const Work w = work_of(p, idx);
+            if (w.e >= 0) {
+              const PrefillEntry& en = p.entries[w.e];
+              d = UnitDesc{en.r, en.q_start, en.q_len, en.seq_len, w.g, w.pair, 1};
+            }
+          }
+        }
+        if (lane == 0) {
+          bar.unit[u & 1] = d;
+          mbar_arrive(&bar.unit_full[u & 1]);
+        }
+        __syncwarp();
+      } else if (!read_unit(u, d)) {
         ok = false;
         break;
       }
-      // ---- where each page box of the tile comes from. A new position (ctx <= pos <
-      // seq) whose slot is its own holds k_new's row after this step, so it is read from
-      // k_new; any other position from the cache (not written in this step). Tiles of
-      // context only (the common case) skip the test: this warp's issue rate bounds the
-      // ring's refill rate.
-      const bool tile_new = fuse && key_base + kKeys > ctx && key_base < seq;  // warp-uniform
-      unsigned bad[4] = {0u, 0u, 0u, 0u};  // bit kk: key key_base + kk is new, slot not its own
-      int src = 0;  // lane i < ppt: page i from 0: the cache (or zeros past the request),
-                    // 1: a box of k_new rows, 2: row by row (straddles ctx or foreign slot)
-      unsigned gen = 0u;
-      if (tile_new) {
+      if (!d.live) break;
+      const Geo e = geo_of(d, TQ, W);
+      const int g = e.g, q_start = e.q_start, seq = e.seq, ctx = e.ctx, kt0 = e.kt0, nkt = e.nkt;
+      const int npages_req = (seq + BS - 1) / BS;
+      const int32_t* bt = p.a.block_table + (long long)e.r * p.a.bt_stride;
+      // page ids of key tile j (lane i < ppt: page i of the tile); checked where
+      // they are used, so that the load of the next tile's ids does not stall
+      auto tile_pages = [&](int j) -> int {
+        const int lp = (((kt0 + j) * kKeys) >> lg_bs) + lane;
+        return (lane < ppt && lp < npages_req) ? __ldg(bt + bt_entry(lp, p.a.ring_blocks)) : 0;
+      };
+      // slot_mapping entries of tile j's keys lane + 32 q that are this step's new
+      // positions (ctx <= pos < seq); -1 elsewhere
+      auto tile_slots = [&](int j, long long (&sl)[4]) {
+        const int key_base = (kt0 + j) * kKeys;
+        if (!(fuse && key_base + kKeys > ctx && key_base < seq)) return;  // no new position
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const int kk = lane + 32 * q4;
-          const int pos = key_base + kk;
-          const int pgk = __shfl_sync(0xffffffffu, ids_cur, (kk >> lg_box) & 31);
-          const bool isnew = pos >= ctx && pos < seq;
-          bad[q4] = __ballot_sync(0xffffffffu,
-                                  isnew && sl_cur[q4] != (long long)pgk * BS + (pos & bs_mask));
+          const int pos = key_base + lane + 32 * q4;
+          sl[q4] = (pos >= ctx && pos < seq) ? __ldg(p.slot_mapping + q_start + (pos - ctx)) : -1;
         }
-        const int kp = key_base + (lane << lg_box);
-        if (lane < ppt && kp < seq && kp + box > ctx) {
-          bool pbad = false;
-#pragma unroll
-          for (int w4 = 0; w4 < 4; ++w4) {
-            const int lo = max(lane << lg_box, 32 * w4), hi = min((lane << lg_box) + box, 32 * w4 + 32);
-            if (lo < hi) {
-              const unsigned bits = bad[w4] >> (lo - 32 * w4);
-              pbad |= (hi - lo == 32 ? bits : (bits & ((1u << (hi - lo)) - 1u))) != 0u;
-            }
-          }
-          src = (kp >= ctx && !pbad) ? 1 : 2;
+      };
+      int ids_cur = tile_pages(0);
+      long long sl_cur[4], sl_next[4];
+      tile_slots(0, sl_cur);
+      if (!is_v) {
+        // the two query tiles: box (64 of D, the G heads of KV head g, TQ tokens) per tile
+        // and half of D lands as the tile's 128 rows (token-major, head-minor) in the
+        // 128B-swizzled K-major layout the products read; tokens past the request are
+        // never output rows (past T they read as zeros). The buffer is free once the
+        // previous unit's last S product is complete.
+        if (u >= 1 && !mbar_wait_warp_or_abort(&bar.q_empty, (uint32_t)((u - 1) & 1), &bar.abort)) {
+          ok = false;
+          break;
         }
-        gen = __ballot_sync(0xffffffffu, src == 2);
-      }
-      if (gen != 0u) {
-        // row by row: 16-byte chunks e = lane + 32 m of (row, half, chunk), loads first
-        constexpr int kBatch = 8;
-        for (unsigned m = gen; m != 0u; m &= m - 1u) {
-          const int pi = __ffs(m) - 1;
-          const int pg = __shfl_sync(0xffffffffu, ids_cur, pi);
-          const int kpi = key_base + pi * box;
-          const bool pg_ok = pg >= 0 && pg < p.a.num_blocks;
-          const int nchunks = box * kHalves * 8;
-          for (int e0 = 0; e0 < nchunks; e0 += 32 * kBatch) {
-            uint4 v[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-              const int e = e0 + lane + 32 * u;
-              const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
-              const int pos = kpi + row;
-              v[u] = make_uint4(0u, 0u, 0u, 0u);
-              if (e < nchunks && pos < seq) {
-                const int kk = pos - key_base;
-                const unsigned bw = kk < 32 ? bad[0] : kk < 64 ? bad[1] : kk < 96 ? bad[2] : bad[3];
-                const bool own = pos >= ctx && ((bw >> (kk & 31)) & 1u) == 0u;
-                if (own) {
-                  v[u] = __ldg(new_rows + (((long long)(q_start + pos - ctx) * Hkv + g) * D + h * 64) / 8 + c);
-                } else if (pg_ok) {
-                  v[u] = __ldg(cache + (((long long)pg * BS + (pos & bs_mask)) * Hkv + g) * (D / 8) + h * 8 + c);
-                } else if (c == 0 && h == 0) {
-                  record_error(p.a.error_word, 0x1);
-                }
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-              const int e = e0 + lane + 32 * u;
-              const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
-              const int trow = pi * box + row;  // row within the tile
-              if (e < nchunks)
-                *reinterpret_cast<uint4*>(dst + h * kHalfBytes + trow * 128 + ((c ^ (trow & 7)) << 4)) = v[u];
-            }
-          }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar.q_full, (uint32_t)((e.has_b ? 2 : 1) * kTile));
+          for (int t = 0; t < (e.has_b ? 2 : 1); ++t)
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_3d(sQ + t * kTile + h * kHalfBytes, &tmap_q, &bar.q_full, h * 64, g * G,
+                          q_start + (e.qt0 + t) * TQ);
+          bar.q_loads = u + 1;  // read by the drain after the CTA's final barrier
         }
-        // the tensor cores read these rows through the async proxy
-        fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        const int tma_bytes = kTile - __popc(gen) * kHalves * box * 128;
-        mbar_arrive_expect_tx(&bar.full[s], (uint32_t)tma_bytes);
-        bar.issued[s] = i;  // read by the drain after the CTA's final barrier
-      }
-      __syncwarp();  // the expect_tx is registered first
-      {
-        // lane b < nbox loads box b (page b / kHalves, half b % kHalves of head_dim); a
-        // page past the request, or past the pool, reads as zeros
-        const int key0 = BS > kKeys ? (key_base & bs_mask) : 0;
-        const int page = lane / kHalves;
-        const int half = lane % kHalves;
-        int pgb = __shfl_sync(0xffffffffu, ids_cur, page & 31);
-        const int srcb = tile_new ? __shfl_sync(0xffffffffu, src, page & 31) : 0;
-        if (lane < nbox && srcb != 2) {
-          uint8_t* bdst = dst + half * kHalfBytes + page * box * 128;
-          if (srcb == 1) {
-            tma_load_3d(bdst, nmap, &bar.full[s], half * 64, g, q_start + (key_base + (page << lg_box) - ctx));
-          } else {
-            if ((((kt0 + j) * kKeys) >> lg_bs) + page >= npages_req) {
-              pgb = p.a.num_blocks;
-            } else if (pgb < 0 || pgb >= p.a.num_blocks) {
-              record_error(p.a.error_word, 0x1);
-              pgb = p.a.num_blocks;
+      for (int j = 0; j < nkt; ++j) {
+        const int i = i_base + 2 * j + is_v;
+        const int s = i % kStages;
+        uint8_t* dst = sRing + s * kTile;
+        const int key_base = (kt0 + j) * kKeys;
+        // the next tile's page ids and slots are read while this one waits for its slot
+        const int ids_next = j + 1 < nkt ? tile_pages(j + 1) : 0;
+        if (j + 1 < nkt) tile_slots(j + 1, sl_next);
+        if (i >= kStages &&
+            !mbar_wait_warp_or_abort(&bar.empty[s], (uint32_t)(((i / kStages) - 1) & 1), &bar.abort)) {
+          ok = false;
+          break;
+        }
+        // ---- where each page box of the tile comes from. A new position (ctx <= pos <
+        // seq) whose slot is its own holds k_new's row after this step, so it is read from
+        // k_new; any other position from the cache (not written in this step). Tiles of
+        // context only (the common case) skip the test: this warp's issue rate bounds the
+        // ring's refill rate.
+        const bool tile_new = fuse && key_base + kKeys > ctx && key_base < seq;  // warp-uniform
+        unsigned bad[4] = {0u, 0u, 0u, 0u};  // bit kk: key key_base + kk is new, slot not its own
+        int src = 0;  // lane i < ppt: page i from 0: the cache (or zeros past the request),
+                      // 1: a box of k_new rows, 2: row by row (straddles ctx or foreign slot)
+        unsigned gen = 0u;
+        if (tile_new) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int kk = lane + 32 * q4;
+            const int pos = key_base + kk;
+            const int pgk = __shfl_sync(0xffffffffu, ids_cur, (kk >> lg_box) & 31);
+            const bool isnew = pos >= ctx && pos < seq;
+            bad[q4] = __ballot_sync(0xffffffffu,
+                                    isnew && sl_cur[q4] != (long long)pgk * BS + (pos & bs_mask));
+          }
+          const int kp = key_base + (lane << lg_box);
+          if (lane < ppt && kp < seq && kp + box > ctx) {
+            bool pbad = false;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const int lo = max(lane << lg_box, 32 * w4), hi = min((lane << lg_box) + box, 32 * w4 + 32);
+              if (lo < hi) {
+                const unsigned bits = bad[w4] >> (lo - 32 * w4);
+                pbad |= (hi - lo == 32 ? bits : (bits & ((1u << (hi - lo)) - 1u))) != 0u;
+              }
             }
-            tma_load_4d(bdst, map, &bar.full[s], half * 64, key0, g, pgb);
+            src = (kp >= ctx && !pbad) ? 1 : 2;
+          }
+          gen = __ballot_sync(0xffffffffu, src == 2);
+        }
+        if (gen != 0u) {
+          // row by row: 16-byte chunks e = lane + 32 m of (row, half, chunk), loads first
+          constexpr int kBatch = 8;
+          for (unsigned m = gen; m != 0u; m &= m - 1u) {
+            const int pi = __ffs(m) - 1;
+            const int pg = __shfl_sync(0xffffffffu, ids_cur, pi);
+            const int kpi = key_base + pi * box;
+            const bool pg_ok = pg >= 0 && pg < p.a.num_blocks;
+            const int nchunks = box * kHalves * 8;
+            for (int e0 = 0; e0 < nchunks; e0 += 32 * kBatch) {
+              uint4 v[kBatch];
+#pragma unroll
+              for (int u = 0; u < kBatch; ++u) {
+                const int e = e0 + lane + 32 * u;
+                const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+                const int pos = kpi + row;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (e < nchunks && pos < seq) {
+                  const int kk = pos - key_base;
+                  const unsigned bw = kk < 32 ? bad[0] : kk < 64 ? bad[1] : kk < 96 ? bad[2] : bad[3];
+                  const bool own = pos >= ctx && ((bw >> (kk & 31)) & 1u) == 0u;
+                  if (own) {
+                    v[u] = __ldg(new_rows + (((long long)(q_start + pos - ctx) * Hkv + g) * D + h * 64) / 8 + c);
+                  } else if (pg_ok) {
+                    v[u] = __ldg(cache + (((long long)pg * BS + (pos & bs_mask)) * Hkv + g) * (D / 8) + h * 8 + c);
+                  } else if (c == 0 && h == 0) {
+                    record_error(p.a.error_word, 0x1);
+                  }
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kBatch; ++u) {
+                const int e = e0 + lane + 32 * u;
+                const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+                const int trow = pi * box + row;  // row within the tile
+                if (e < nchunks)
+                  *reinterpret_cast<uint4*>(dst + h * kHalfBytes + trow * 128 + ((c ^ (trow & 7)) << 4)) = v[u];
+              }
+            }
+          }
+          // the tensor cores read these rows through the async proxy
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const int tma_bytes = kTile - __popc(gen) * kHalves * box * 128;
+          mbar_arrive_expect_tx(&bar.full[s], (uint32_t)tma_bytes);
+          bar.issued[s] = (int)i;  // read by the drain after the CTA's final barrier
+        }
+        __syncwarp();  // the expect_tx is registered first
+        {
+          // lane b < nbox loads box b (page b / kHalves, half b % kHalves of head_dim); a
+          // page past the request, or past the pool, reads as zeros
+          const int key0 = BS > kKeys ? (key_base & bs_mask) : 0;
+          const int page = lane / kHalves;
+          const int half = lane % kHalves;
+          int pgb = __shfl_sync(0xffffffffu, ids_cur, page & 31);
+          const int srcb = tile_new ? __shfl_sync(0xffffffffu, src, page & 31) : 0;
+          if (lane < nbox && srcb != 2) {
+            uint8_t* bdst = dst + half * kHalfBytes + page * box * 128;
+            if (srcb == 1) {
+              tma_load_3d(bdst, nmap, &bar.full[s], half * 64, g, q_start + (key_base + (page << lg_box) - ctx));
+            } else {
+              if ((((kt0 + j) * kKeys) >> lg_bs) + page >= npages_req) {
+                pgb = p.a.num_blocks;
+              } else if (pgb < 0 || pgb >= p.a.num_blocks) {
+                record_error(p.a.error_word, 0x1);
+                pgb = p.a.num_blocks;
+              }
+              tma_load_4d(bdst, map, &bar.full[s], half * 64, key0, g, pgb);
+            }
           }
         }
-      }
-      __syncwarp();
-      ids_cur = ids_next;
+        __syncwarp();
+        ids_cur = ids_next;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) sl_cur[q4] = sl_next[q4];
+        for (int q4 = 0; q4 < 4; ++q4) sl_cur[q4] = sl_next[q4];
+      }
+      if (!ok) break;
+      i_base += 2 * nkt;
     }
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
       set_abort(&bar.abort);
     }
+    teardown();
   } else if (warp == kWarpMma) {
     // =================================================== MMA issuer
     // The whole warp runs this loop (the descriptors stay warp-uniform); one
@@ -477,40 +626,65 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         umma_bf16_tmem_a_elect(tmem + 2 * kKeys + t * D, tmem + t * kKeys + ks * 8,
                                dv + (uint64_t)(ks * (2048 >> 4)), idO, (acc || ks > 0) ? 1u : 0u);
     };
-    ok = mbar_wait_warp_or_abort(&bar.q_full, 0, &bar.abort) && slot_ready(0);
-    if (ok) {
-      tcgen05_fence_after();
-      qk(0, 0);
-      if (has_b) qk(1, 0);
-      umma_commit_elect(&bar.empty[0]);
-    }
-    for (int j = 0; j < nkt && ok; ++j) {
-      const int iv = 2 * j + 1;  // V_j
-      const int ik = 2 * j + 2;  // K_{j+1}
-      const bool more = j + 1 < nkt;
-      // the loads are waited for before P, the one wait that depends on the softmax
-      if (!slot_ready(iv) || (more && !slot_ready(ik)) ||
-          !mbar_wait_warp_or_abort(&bar.p_full[0], (uint32_t)(j & 1), &bar.abort)) {
+    int i_base = 0;
+    int pwaits[kTiles] = {0, 0};  // p_full waits done so far (phase parity)
+    int olive[kTiles] = {0, 0};   // units so far in which query tile t had rows
+    for (int u = 0; ok; ++u) {
+      UnitDesc d;
+      if (!read_unit(u, d)) {
         ok = false;
         break;
       }
+      if (!d.live) break;
+      const Geo e = geo_of(d, TQ, W);
+      const int nkt = e.nkt;
+      const bool has_b = e.has_b;
+      ok = mbar_wait_warp_or_abort(&bar.q_full, (uint32_t)(u & 1), &bar.abort) && slot_ready(i_base);
+      if (!ok) break;
       tcgen05_fence_after();
-      pv(0, iv, j > 0);
-      if (!more) umma_commit_elect(&bar.o_done[0]);
-      if (!has_b) umma_commit_elect(&bar.empty[iv % kStages]);
-      if (more) qk(0, ik);
-      if (has_b) {
-        if (!mbar_wait_warp_or_abort(&bar.p_full[1], (uint32_t)(j & 1), &bar.abort)) {
+      qk(0, i_base);
+      if (has_b) qk(1, i_base);
+      umma_commit_elect(&bar.empty[i_base % kStages]);
+      if (nkt == 1) umma_commit_elect(&bar.q_empty);  // the unit's last S products
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int iv = i_base + 2 * j + 1;  // V_j
+        const int ik = i_base + 2 * j + 2;  // K_{j+1}
+        const bool more = j + 1 < nkt;
+        // the loads are waited for before P, the one wait that depends on the softmax;
+        // before the unit's first PV_t the epilogue of O_t's previous unit must be done
+        if (!slot_ready(iv) || (more && !slot_ready(ik)) ||
+            !mbar_wait_warp_or_abort(&bar.p_full[0], (uint32_t)(pwaits[0]++ & 1), &bar.abort) ||
+            (j == 0 && olive[0] > 0 &&
+             !mbar_wait_warp_or_abort(&bar.o_free[0], (uint32_t)((olive[0] - 1) & 1), &bar.abort))) {
           ok = false;
           break;
         }
         tcgen05_fence_after();
-        pv(1, iv, j > 0);
-        if (!more) umma_commit_elect(&bar.o_done[1]);
-        umma_commit_elect(&bar.empty[iv % kStages]);
-        if (more) qk(1, ik);
+        pv(0, iv, j > 0);
+        if (!more) umma_commit_elect(&bar.o_done[0]);
+        if (!has_b) umma_commit_elect(&bar.empty[iv % kStages]);
+        if (more) qk(0, ik);
+        if (more && !has_b && j + 2 == nkt) umma_commit_elect(&bar.q_empty);
+        if (has_b) {
+          if (!mbar_wait_warp_or_abort(&bar.p_full[1], (uint32_t)(pwaits[1]++ & 1), &bar.abort) ||
+              (j == 0 && olive[1] > 0 &&
+               !mbar_wait_warp_or_abort(&bar.o_free[1], (uint32_t)((olive[1] - 1) & 1), &bar.abort))) {
+            ok = false;
+            break;
+          }
+          tcgen05_fence_after();
+          pv(1, iv, j > 0);
+          if (!more) umma_commit_elect(&bar.o_done[1]);
+          umma_commit_elect(&bar.empty[iv % kStages]);
+          if (more) qk(1, ik);
+          if (more && j + 2 == nkt) umma_commit_elect(&bar.q_empty);
+        }
+        if (more) umma_commit_elect(&bar.empty[ik % kStages]);
       }
-      if (more) umma_commit_elect(&bar.empty[ik % kStages]);
+      if (!ok) break;
+      ++olive[0];
+      if (has_b) ++olive[1];
+      i_base += 2 * nkt;
     }
     if (!ok && lane == 0) {
       record_error(p.a.error_word, 0x4);
@@ -520,35 +694,71 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // commit tracks them all; it completes whether or not the loop ran to its end)
     umma_commit_elect(&bar.drain);
     mbar_wait_warp(&bar.drain, 0);
+    teardown();
   } else {
+    teardown();  // warp 11
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     // =================================================== softmax warpgroups
     const int t = warp >> 2;             // query tile of this group
     const int row = threadIdx.x & (kRows - 1);  // TMEM lane = tile row
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-    const int G = p.a.num_q_heads / p.a.num_kv_heads;
-    const bool tile_live = t == 0 || has_b;
-    const int tok0 = (qt0 + t) * TQ;
-    const int tok = tok0 + row / G;
-    const int hh = row % G;
-    const bool row_valid = tile_live && tok < q_len;
-    if (tile_live) {
-      const int qpos = ctx + tok;
-      const int max_kv = min(qpos, seq - 1);
-      const int min_kv = W > 0 ? max(0, qpos - W + 1) : 0;
+    const uint32_t tS = tmem + lane_addr + t * kKeys;
+    const uint32_t tO = tmem + lane_addr + 2 * kKeys + t * D;
+    int i_base = 0;
+    int swaits = 0;  // s_full[t] waits so far (phase parity)
+    int owaits = 0;  // o_done[t] waits so far
+    for (int u = 0; ok; ++u) {
+      // The unit stays in its ring slot until this group is done with it (the slot is
+      // released at the unit's end), so that its fields are read from shared memory where
+      // they are used instead of being held in registers across the key loop.
+      if (!mbar_wait_warp_or_abort(&bar.unit_full[u & 1], (uint32_t)((u >> 1) & 1), &bar.abort)) {
+        ok = false;
+        break;
+      }
+      const volatile UnitDesc* ud = &bar.unit[u & 1];
+#define CB_UNIT_GEO() geo_of(ud->r, ud->q_start, ud->q_len, ud->seq_len, ud->g, ud->pair, TQ, W)
+#define CB_RELEASE_UNIT()                                 \
+  do {                                                    \
+    __syncwarp();                                         \
+    if (lane == 0) mbar_arrive(&bar.unit_empty[u & 1]);   \
+  } while (0)
+      if (!ud->live) {
+        CB_RELEASE_UNIT();
+        break;
+      }
+      int kt0, nkt, seq, min_kv, max_kv, tile_max_kv_min, tile_min_kv_max;
+      {
+        const Geo e = CB_UNIT_GEO();
+        const int unit_nkt = e.nkt;
+        const bool tile_live = t == 0 || e.has_b;
+        if (!tile_live) {  // this unit has no tile B
+          i_base += 2 * unit_nkt;
+          CB_RELEASE_UNIT();
+          continue;
+        }
+        kt0 = e.kt0;
+        nkt = e.nkt;
+        seq = e.seq;
+        const int tok0 = (e.qt0 + t) * TQ;
+        const int qpos = e.ctx + tok0 + row / G;
+        max_kv = min(qpos, e.seq - 1);
+        min_kv = W > 0 ? max(0, qpos - W + 1) : 0;
+        // keys every row of the tile attends: [tile_min_kv_max, tile_max_kv_min]
+        const int tok_end = min(e.q_len, tok0 + TQ);
+        tile_max_kv_min = min(e.ctx + tok0, e.seq - 1);
+        tile_min_kv_max = W > 0 ? max(0, e.ctx + tok_end - 1 - W + 1) : 0;
+      }
+      i_base += 2 * nkt;
       const float sl2 = p.a.scale_log2;
-      // keys every row of the tile attends: [tile_min_kv_max, tile_max_kv_min]
-      const int tok_end = min(q_len, tok0 + TQ);
-      const int tile_max_kv_min = min(ctx + tok0, seq - 1);
-      const int tile_min_kv_max = W > 0 ? max(0, ctx + tok_end - 1 - W + 1) : 0;
-      const uint32_t tS = tmem + lane_addr + t * kKeys;
-      const uint32_t tO = tmem + lane_addr + 2 * kKeys + t * D;
       float m_ref = -FLT_MAX;
       float l = 0.f;
       // test hook: the group's first wait runs out (nothing arrives at bar.never)
-      if (p.a.test_expire_wait && !mbar_wait_warp_polls(&bar.never, 0, kTestExpiryPolls))
+      if (u == 0 && p.a.test_expire_wait && !mbar_wait_warp_polls(&bar.never, 0, kTestExpiryPolls))
         ok = false;
       for (int j = 0; j < nkt && ok; ++j) {
-        if (!mbar_wait_warp_or_abort(&bar.s_full[t], (uint32_t)(j & 1), &bar.abort)) {
+        if (!mbar_wait_warp_or_abort(&bar.s_full[t], (uint32_t)(swaits++ & 1), &bar.abort)) {
           ok = false;
           break;
         }
@@ -618,7 +828,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // Each group does it before its own P is signalled (the other group may
         // write the same zeros at the same time), so before either PV reads V.
         if (key_base + kKeys > seq) {
-          const int iv = 2 * j + 1;
+          const int iv = i_base - 2 * (nkt - j) + 1;  // V_j of this unit
           if (!mbar_wait_warp_or_abort(&bar.full[iv % kStages], (uint32_t)((iv / kStages) & 1),
                                        &bar.abort)) {
             ok = false;
@@ -640,7 +850,13 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) mbar_arrive(&bar.p_full[t]);
       }
       // ---- epilogue: O / l for the rows of this tile
-      if (ok && !mbar_wait_warp_or_abort(&bar.o_done[t], 0, &bar.abort)) ok = false;
+      if (ok && !mbar_wait_warp_or_abort(&bar.o_done[t], (uint32_t)(owaits++ & 1), &bar.abort))
+        ok = false;
+      const Geo e = CB_UNIT_GEO();
+      const int g = e.g, q_start = e.q_start;
+      const int tok = (e.qt0 + t) * TQ + row / G;
+      const int hh = row % G;
+      const bool row_valid = tok < e.q_len;
       if (ok) {
         tcgen05_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -663,83 +879,82 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
           }
         }
+        // O_t is read: the next unit's products may overwrite it
+        tcgen05_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar.o_free[t]);
       } else if (lane == 0) {
         record_error(p.a.error_word, 0x4);
         set_abort(&bar.abort);
       }
-      // ---- the new K and V rows of this CTA's tokens for KV head g to their slots (a slot
-      // below zero is skipped, one past the pool recorded and skipped), after the CTA's
-      // attention work so that the copy does not compete with it. The tile pairs of all
-      // KV heads cover every (token, head) of the request once; nothing in the step reads
-      // these positions from the cache (the TMA warps read them from k_new).
-      if (p.k_new != nullptr) {
-        constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
-        constexpr int kPerTok = 2 * kRowChunks;
-        const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
-        const int Hkv = p.a.num_kv_heads;
-        const int nthr = has_b ? kSoftmaxThreads : kRows;
-        const int me = t * kRows + row;
-        const int n = (cta_tok_end - cta_tok0) * kPerTok;
-        constexpr int kBatch = 8;
-        for (int e0 = 0; e0 < n; e0 += nthr * kBatch) {
+      if (!ok) break;
+      CB_RELEASE_UNIT();
+    }
+#undef CB_UNIT_GEO
+#undef CB_RELEASE_UNIT
+    if (!ok && lane == 0) {
+      record_error(p.a.error_word, 0x4);
+      set_abort(&bar.abort);
+    }
+    // ---- the step's new K and V rows to their slots (a slot below zero is skipped, one
+    // past the pool recorded and skipped). Nothing in the step reads these positions from
+    // the cache (the TMA warps read them from k_new), so the copy may run at any time: the
+    // softmax warps of CTAs with no attention work left claim it a quarter of a unit's
+    // tokens for its KV head at a time, so that it runs while the longest units compute
+    // and competes with no product of its own CTA. The parts of all units cover every
+    // (token, KV head) of the listed requests once.
+    if (ok && p.k_new != nullptr && !p.device_work) {
+      constexpr int kParts = 4;
+      constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
+      constexpr int kPerTok = 2 * kRowChunks;
+      static_assert(32 % kPerTok == 0 || kPerTok == 32, "a lane keeps one chunk of the row");
+      constexpr int kTokPass = 32 / kPerTok;  // tokens per pass of the warp
+      constexpr int kBatch = 8;
+      const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
+      const int rem = lane % kPerTok;  // the same 16-byte chunk of every token it copies
+      const int sub = lane / kPerTok;
+      const int per = kTiles * TQ / kParts;  // TQ = 128 / G tokens, so 4 or more per part
+      const int n_parts = p.total_units * kParts;
+      for (;;) {
+        int it = 0;
+        if (lane == 0) it = atomicAdd(p.scatter_counter, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (it >= n_parts) break;
+        const Work w = work_of(p, it / kParts);
+        if (w.e < 0) continue;
+        const PrefillEntry& en = p.entries[w.e];
+        const int a0 = kTiles * w.pair * TQ + (it % kParts) * per;
+        const int ntok = min(en.q_len - a0, per);
+        const uint4* src = static_cast<const uint4*>(rem < kRowChunks ? p.k_new : p.v_new) +
+                           (long long)w.g * kRowChunks + rem % kRowChunks;
+        uint4* dst = static_cast<uint4*>(rem < kRowChunks ? p.a.k_cache : p.a.v_cache) +
+                     (long long)w.g * kRowChunks + rem % kRowChunks;
+        const long long tk_first = (long long)en.q_start + a0;
+        for (int k0 = sub; k0 < ntok; k0 += kTokPass * kBatch) {
           uint4 v[kBatch];
           long long sl[kBatch];
 #pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const int e = e0 + me + nthr * u;
-            sl[u] = -1;
-            if (e < n) {
-              const long long tok = q_start + cta_tok0 + e / kPerTok;
-              const int rem = e % kPerTok;
-              const uint4* src = static_cast<const uint4*>(rem < kRowChunks ? p.k_new : p.v_new);
-              sl[u] = __ldg(p.slot_mapping + tok);
-              v[u] = __ldg(src + (tok * Hkv + g) * kRowChunks + rem % kRowChunks);
+          for (int b = 0; b < kBatch; ++b) {
+            const int k = k0 + kTokPass * b;
+            sl[b] = -1;
+            if (k < ntok) {
+              sl[b] = __ldg(p.slot_mapping + tk_first + k);
+              v[b] = __ldg(src + (tk_first + k) * (Hkv * kRowChunks));
             }
           }
 #pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const int e = e0 + me + nthr * u;
-            if (e < n && sl[u] >= 0) {
-              const int rem = e % kPerTok;
-              if (sl[u] < num_slots) {
-                uint4* dstc = static_cast<uint4*>(rem < kRowChunks ? p.a.k_cache : p.a.v_cache);
-                dstc[(sl[u] * Hkv + g) * kRowChunks + rem % kRowChunks] = v[u];
-              } else if (rem == 0) {
+          for (int b = 0; b < kBatch; ++b) {
+            if (sl[b] >= 0) {
+              if (sl[b] < num_slots)
+                dst[sl[b] * (Hkv * kRowChunks)] = v[b];
+              else if (rem == 0)
                 record_error(p.a.error_word, 0x2);
-              }
             }
           }
         }
       }
     }
-  }
-
-  // ---- teardown: every tcgen05 access is complete before the columns are freed
-  tcgen05_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tcgen05_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-  // If a wait gave up, copies may be in flight that no MMA consumed. The ring's slots
-  // are filled in index order and a slot is refilled only after its previous copy was
-  // consumed, so only the latest copy of each slot can be in flight: waiting for its
-  // phase drains the ring before the CTA's shared memory is released.
-  if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&bar.abort)) {
-    mbar_wait(&bar.q_full, 0);  // the query tiles' copies
-    for (int s2 = 0; s2 < kStages; ++s2) {
-      const int i = bar.issued[s2];
-      if (i >= 0) mbar_wait(&bar.full[s2], (uint32_t)((i / kStages) & 1));
-    }
-  }
-  // Launched beside the decode kernel: the last CTA to finish waits for the decode
-  // grid, so that this grid completes only after it (the combine launch that follows
-  // waits for this grid and reads the decode partials), and resets the counter.
-  if (p.concurrent && threadIdx.x == 0) {
-    if (atomicAdd(p.exit_counter, 1) == p.total_ctas - 1) {
-      atomicExch(p.exit_counter, 0);
-      grid_dependency_wait();
-    }
+    teardown();
   }
 }
 
@@ -812,12 +1027,18 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
   static bool attr_set = false;
   constexpr size_t smem = smem_bytes<D>();
   if (!attr_set) {
+    // the register split inside the kernel assumes kRegsLaunch registers per thread at
+    // launch; with fewer, the softmax warps' increase would wait for registers forever
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     attr_set = true;
   }
-  return launch_pdl(kPrefillTc, kern, dim3(p.total_ctas), dim3(kThreads), smem, s, mk, mv, mkn,
-                    mvn, mq, p);
+  return launch_pdl(kPrefillTc, kern, dim3(p.grid), dim3(kThreads), smem, s, mk, mv, mkn, mvn,
+                    mq, p);
 }
 
 }  // namespace
@@ -847,7 +1068,7 @@ cudaError_t prepare_prefill(int head_dim) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream) {
-  if (p.total_ctas <= 0) return cudaSuccess;
+  if (p.grid <= 0) return cudaSuccess;
   if (p.a.head_dim == 64) return launch_d<64>(p, stream);
   return launch_d<128>(p, stream);
 }

@@ -219,6 +219,9 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
       pa.slot_mapping = plan.fused_scatter ? scatter->slot_mapping : nullptr;
       pa.concurrent = plan.concurrent ? 1 : 0;
       pa.exit_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kExitCounterOffset);
+      pa.unit_counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kUnitCounterOffset);
+      pa.scatter_counter =
+          reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kScatterCounterOffset);
       for (size_t i = (size_t)l * kPrefillMaxEntries;
            i < order.size() && pa.n_entries < kPrefillMaxEntries; ++i) {
         const int r = order[i].second;
@@ -231,6 +234,9 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
         e.seq_len = h_seq_lens[r];
         pa.total_ctas += prefill_ctas(e.n_qtiles, a.num_kv_heads);
       }
+      // persistent CTAs, one per SM at most, claim the units heaviest first
+      pa.total_units = pa.total_ctas;
+      pa.grid = std::min(pa.total_units, sm_count());
       prefill_total_ctas += pa.total_ctas;
     }
     plan.n_prefill_launches = n_launch;
@@ -371,9 +377,13 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   pa.slot_mapping = nullptr;
   pa.concurrent = 0;
   pa.exit_counter = nullptr;
+  pa.unit_counter = nullptr;
+  pa.scatter_counter = nullptr;
   pa.device_work = 1;
   pa.total_ctas = prefill_ctas_bound(a.num_tokens, a.num_requests, pa.tile_tokens,
                                      a.num_kv_heads);
+  pa.total_units = pa.total_ctas;
+  pa.grid = pa.total_ctas;  // one unit per CTA, found on the device
   plan.n_prefill_launches = with_prefill ? 1 : 0;
   plan.fast_prefill = with_prefill;
   return true;

@@ -13,6 +13,8 @@ namespace cb {
 
 constexpr size_t kWorkspaceHeaderBytes = 256;  // error word, prefill exit counter, reserved
 constexpr size_t kExitCounterOffset = 64;      // int: prefill CTAs finished (zero between steps)
+constexpr size_t kUnitCounterOffset = 128;     // int: prefill units claimed (zero between steps)
+constexpr size_t kScatterCounterOffset = 192;  // int: prefill row-copy parts claimed (likewise)
 constexpr int kMaxDecodeCtas = 2048;           // upper bound on decode CTAs (workspace sizing)
 constexpr int kMaxPrefillLaunches = 8;         // x kPrefillMaxEntries prefill requests per step
 

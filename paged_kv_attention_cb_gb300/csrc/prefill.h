@@ -41,13 +41,18 @@ struct PrefillArgs {
   // wait for them; the last of its CTAs to finish waits for the decode grid, so that the
   // completion of this grid implies the decode grid's (the combine launch that follows
   // reads the decode partials). exit_counter: an int in the workspace header, zero
-  // between steps.
+  // between steps (the last CTA also resets unit_counter through it).
   int concurrent;
   int* exit_counter;
   int device_work;     // entries unused: each CTA finds its work in the device metadata (graph
                        // replays: nothing in the arguments depends on the batch); total_ctas is
                        // then an upper bound and the CTAs past the step's work exit at once
-  int total_ctas;    // sum over entries of prefill_ctas(n_qtiles, Hkv)
+  int total_ctas;    // units: sum over entries of prefill_ctas(n_qtiles, Hkv) (an upper bound
+                     // with device_work)
+  int total_units;   // units of the list (CTAs claim them through unit_counter)
+  int grid;          // CTAs launched: min(units, SMs); with device_work one per unit (bound)
+  int* unit_counter; // next unit of the list to claim (workspace header, zero between steps)
+  int* scatter_counter;  // next part of the new-row copy to claim (likewise)
   PrefillEntry entries[kPrefillMaxEntries];  // heaviest first
 };
 

@@ -286,6 +286,18 @@ CB_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 
+// Register reallocation between warpgroups: every warp of the warpgroup executes it. An
+// increase waits until the registers are free in the CTA's pool (the threads x registers
+// it was launched with), so the warpgroups' shares must add up to at most that.
+template <uint32_t N>
+CB_DEV void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+CB_DEV void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 CB_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 CB_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

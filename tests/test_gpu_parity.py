@@ -357,6 +357,24 @@ def test_prefill_chunks_with_context(D, window):
     full_check(spec)
 
 
+def test_prefill_requests_over_several_launches_repeat_bitwise():
+    """More prompt requests than one prefill launch lists: the launches of a step claim
+    their units from one counter in the workspace header, which each launch's last CTA
+    sets back to zero, so a second run of the step on the same workspace is bitwise equal."""
+    rng = np.random.default_rng(23)
+    n = 300
+    q_lens = [int(x) for x in rng.integers(2, 10, n)]
+    ctx = [int(x) for x in rng.integers(0, 300, n)]
+    spec = workloads.custom(q_lens, ctx, num_q_heads=8, num_kv_heads=2, block_size=16, seed=23)
+    full_check(spec)
+    st = GpuStep(spec)
+    first = st.run().clone()
+    again = st.run()
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) == 0
+    assert torch.equal(first, again)
+
+
 def test_prefill_fast_equals_portable_path():
     spec = workloads.custom([1, 70, 1, 200], [90, 400, 3, 0], num_q_heads=32, num_kv_heads=8,
                             seed=17)
