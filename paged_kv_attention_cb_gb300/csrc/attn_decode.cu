@@ -30,10 +30,11 @@
 //   the request's query rows arrive by a 1-D bulk copy into a 2-slot ring.
 // * Contraction. Per warp and block: S^T (16 keys x 8 heads) = K Q^T and
 //   O^T (D x 8 heads) += V^T P^T on mma.sync m16n8k16 (bf16 in, fp32
-//   accumulate); the key axis is the M dimension so a group of G <= 8 query
-//   heads fills the N = 8 columns. P^T goes from the accumulator layout to the
-//   B-operand layout with movmatrix. Softmax statistics are per column, kept
-//   per lane and reduced with warp shuffles.
+//   accumulate); the key axis is the M dimension so a group of up to 8 query
+//   heads fills the N = 8 columns (G = 16: two such column blocks, sharing each
+//   K and V fragment). P^T goes from the accumulator layout to the B-operand
+//   layout with movmatrix. Softmax statistics are per column, kept per lane and
+//   reduced with warp shuffles.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <float.h>
@@ -124,7 +125,8 @@ __global__ void __launch_bounds__(kDecodeMaxHeads * 32 + 32, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs p) {
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(G >= 1 && G <= 8, "group");
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "group");
+  constexpr int NB = (G + 7) / 8;  // 8-head column blocks
   constexpr int kHalves = D / 64;
   constexpr int kKSteps = D / 16;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
@@ -482,24 +484,31 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         lane % kRowChunks);
       }
     }
-    // query fragments (B operand of S^T = K Q^T): Q[head = gid][d = 16ks + 2tq (+8)]
-    uint32_t qf[kKSteps][2];
-    {
+    // query fragments (B operand of S^T = K Q^T): Q[head = 8 nb + gid][d = 16ks + 2tq (+8)]
+    uint32_t qf[NB][kKSteps][2];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const int head = 8 * nb + gid;
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qring + qs * p.q_slot_bytes +
-                                                               (hl * G + gid) * D * 2);
+                                                               (hl * G + head) * D * 2);
 #pragma unroll
       for (int ks = 0; ks < kKSteps; ++ks) {
-        qf[ks][0] = gid < G ? qrow[(16 * ks + 2 * tq) >> 1] : 0u;
-        qf[ks][1] = gid < G ? qrow[(16 * ks + 2 * tq + 8) >> 1] : 0u;
+        qf[nb][ks][0] = head < G ? qrow[(16 * ks + 2 * tq) >> 1] : 0u;
+        qf[nb][ks][1] = head < G ? qrow[(16 * ks + 2 * tq + 8) >> 1] : 0u;
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.qempty[qs]);
 
-    float o[kKSteps][4];
+    float o[NB][kKSteps][4];
+    float m0[NB], m1[NB], l0[NB], l1[NB];
 #pragma unroll
-    for (int m = 0; m < kKSteps; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
-    float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f;
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int m = 0; m < kKSteps; ++m) o[nb][m][0] = o[nb][m][1] = o[nb][m][2] = o[nb][m][3] = 0.f;
+      m0[nb] = m1[nb] = -FLT_MAX;
+      l0[nb] = l1[nb] = 0.f;
+    }
 
     for (int kb = d.kb0; kb < d.kb1; ++kb, ++i) {
       const int s = (int)(i % p.stages);
@@ -547,8 +556,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         fence_proxy_async_smem();  // as above: before the stage is handed back to the copies
         __syncwarp();
       }
-      // ---- S^T = K Q^T  (16 keys x 8 heads)
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T = K Q^T  (16 keys x 8 heads per column block)
+      float sacc[NB][4];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
       {
         const int jm = lane >> 3;
         const int key = (lane & 7) + ((jm & 1) << 3);
@@ -558,42 +569,47 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           const int chunk = (ks & 3) * 2 + (jm >> 1);
           uint32_t a[4];
           ldmatrix_x4(a, row_addr + (ks >> 2) * box_bytes + ((chunk ^ (key & 7)) << 4));
-          mma_bf16_16816(sacc, a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(sacc[nb], a, qf[nb][ks][0], qf[nb][ks][1]);
         }
       }
-      // ---- mask, online softmax per head column (2tq, 2tq+1)
+      // ---- mask, online softmax per head column (8 nb + 2tq, 8 nb + 2tq + 1)
       const int k0 = key_base + gid;
       const int k1 = k0 + 8;
       const bool v0 = k0 >= d.lo && k0 <= d.hi;
       const bool v1 = k1 >= d.lo && k1 <= d.hi;
-      const float s0 = v0 ? sacc[0] * sl2 : -INFINITY;
-      const float s1 = v0 ? sacc[1] * sl2 : -INFINITY;
-      const float s2 = v1 ? sacc[2] * sl2 : -INFINITY;
-      const float s3 = v1 ? sacc[3] * sl2 : -INFINITY;
-      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+      uint32_t pb0[NB], pb1[NB];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
-      const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      l0 = l0 * a0 + (p0 + p2);
-      l1 = l1 * a1 + (p1 + p3);
+      for (int nb = 0; nb < NB; ++nb) {
+        const float s0 = v0 ? sacc[nb][0] * sl2 : -INFINITY;
+        const float s1 = v0 ? sacc[nb][1] * sl2 : -INFINITY;
+        const float s2 = v1 ? sacc[nb][2] * sl2 : -INFINITY;
+        const float s3 = v1 ? sacc[nb][3] * sl2 : -INFINITY;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-      for (int m = 0; m < kKSteps; ++m) {
-        o[m][0] *= a0;
-        o[m][1] *= a1;
-        o[m][2] *= a0;
-        o[m][3] *= a1;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0[nb], mx0), mn1 = fmaxf(m1[nb], mx1);
+        const float a0 = exp2f(m0[nb] - mn0), a1 = exp2f(m1[nb] - mn1);
+        const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+        const float p2 = exp2f(s2 - mn0), p3 = exp2f(s3 - mn1);
+        m0[nb] = mn0;
+        m1[nb] = mn1;
+        l0[nb] = l0[nb] * a0 + (p0 + p2);
+        l1[nb] = l1[nb] * a1 + (p1 + p3);
+#pragma unroll
+        for (int m = 0; m < kKSteps; ++m) {
+          o[nb][m][0] *= a0;
+          o[nb][m][1] *= a1;
+          o[nb][m][2] *= a0;
+          o[nb][m][3] *= a1;
+        }
+        pb0[nb] = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
+        pb1[nb] = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
       }
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // keys 0-7
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // keys 8-15
-      // ---- O^T += V^T P^T  (D x 8 heads)
+      // ---- O^T += V^T P^T  (D x 8 heads per column block)
       {
         const int jm = lane >> 3;
         const int key = (lane & 7) + ((jm >> 1) << 3);
@@ -604,7 +620,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           uint32_t a[4];
           ldmatrix_x4_trans(a, row_addr + (chunk >> 3) * box_bytes +
                                    (((chunk & 7) ^ (key & 7)) << 4));
-          mma_bf16_16816(o[m], a, pb0, pb1);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(o[nb][m], a, pb0[nb], pb1[nb]);
         }
       }
       __syncwarp();
@@ -612,46 +629,50 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 
     // ---- segment epilogue
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    const int h0 = 2 * tq, h1 = 2 * tq + 1;
     const int qh_base = (hg * HB + hl) * G;
-    if (d.direct) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems;
-      const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
-      for (int m = 0; m < kKSteps; ++m) {
-        const int dd = 16 * m + gid;
-        if (h0 < G) {
-          out[(qh_base + h0) * D + dd] = __float2bfloat16_rn(o[m][0] * i0);
-          out[(qh_base + h0) * D + dd + 8] = __float2bfloat16_rn(o[m][2] * i0);
-        }
-        if (h1 < G) {
-          out[(qh_base + h1) * D + dd] = __float2bfloat16_rn(o[m][1] * i1);
-          out[(qh_base + h1) * D + dd + 8] = __float2bfloat16_rn(o[m][3] * i1);
-        }
-      }
-    } else {
-      float* po = p.part_o + (long long)d.slot * q_row_elems;
+    for (int nb = 0; nb < NB; ++nb) {
+      float sl0 = l0[nb], sl1 = l1[nb];
 #pragma unroll
-      for (int m = 0; m < kKSteps; ++m) {
-        const int dd = 16 * m + gid;
-        if (h0 < G) {
-          po[(qh_base + h0) * D + dd] = o[m][0];
-          po[(qh_base + h0) * D + dd + 8] = o[m][2];
-        }
-        if (h1 < G) {
-          po[(qh_base + h1) * D + dd] = o[m][1];
-          po[(qh_base + h1) * D + dd + 8] = o[m][3];
-        }
+      for (int off = 4; off < 32; off <<= 1) {
+        sl0 += __shfl_xor_sync(0xffffffffu, sl0, off);
+        sl1 += __shfl_xor_sync(0xffffffffu, sl1, off);
       }
-      if (gid == 0) {
-        float2* pml = p.part_ml + (long long)d.slot * p.a.num_q_heads;
-        if (h0 < G) pml[qh_base + h0] = make_float2(m0, l0);
-        if (h1 < G) pml[qh_base + h1] = make_float2(m1, l1);
+      const int h0 = 8 * nb + 2 * tq, h1 = h0 + 1;
+      if (d.direct) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + (long long)d.t * q_row_elems;
+        const float i0 = 1.f / sl0, i1 = 1.f / sl1;
+#pragma unroll
+        for (int m = 0; m < kKSteps; ++m) {
+          const int dd = 16 * m + gid;
+          if (h0 < G) {
+            out[(qh_base + h0) * D + dd] = __float2bfloat16_rn(o[nb][m][0] * i0);
+            out[(qh_base + h0) * D + dd + 8] = __float2bfloat16_rn(o[nb][m][2] * i0);
+          }
+          if (h1 < G) {
+            out[(qh_base + h1) * D + dd] = __float2bfloat16_rn(o[nb][m][1] * i1);
+            out[(qh_base + h1) * D + dd + 8] = __float2bfloat16_rn(o[nb][m][3] * i1);
+          }
+        }
+      } else {
+        float* po = p.part_o + (long long)d.slot * q_row_elems;
+#pragma unroll
+        for (int m = 0; m < kKSteps; ++m) {
+          const int dd = 16 * m + gid;
+          if (h0 < G) {
+            po[(qh_base + h0) * D + dd] = o[nb][m][0];
+            po[(qh_base + h0) * D + dd + 8] = o[nb][m][2];
+          }
+          if (h1 < G) {
+            po[(qh_base + h1) * D + dd] = o[nb][m][1];
+            po[(qh_base + h1) * D + dd + 8] = o[nb][m][3];
+          }
+        }
+        if (gid == 0) {
+          float2* pml = p.part_ml + (long long)d.slot * p.a.num_q_heads;
+          if (h0 < G) pml[qh_base + h0] = make_float2(m0[nb], sl0);
+          if (h1 < G) pml[qh_base + h1] = make_float2(m1[nb], sl1);
+        }
       }
     }
   }
@@ -887,6 +908,7 @@ cudaError_t launch_d(const DecodeArgs& p, const CUtensorMap& mk, const CUtensorM
     case 2: return launch_dg<D, 2>(p, mk, mv, smem, hg, R, s);
     case 4: return launch_dg<D, 4>(p, mk, mv, smem, hg, R, s);
     case 8: return launch_dg<D, 8>(p, mk, mv, smem, hg, R, s);
+    case 16: return launch_dg<D, 16>(p, mk, mv, smem, hg, R, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -899,6 +921,7 @@ cudaError_t launch_combine_d(const CombineArgs& c, dim3 grid, dim3 block, size_t
     case 2: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 2>, grid, block, smem, s, c);
     case 4: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 4>, grid, block, smem, s, c);
     case 8: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 8>, grid, block, smem, s, c);
+    case 16: return launch_pdl(kDecodeCombine, decode_combine_kernel<D, 16>, grid, block, smem, s, c);
   }
   return cudaErrorInvalidValue;
 }
@@ -937,6 +960,7 @@ cudaError_t prepare_decode(const DecodeArgs& p) {
       case 2: return set(decode_split_kernel<64, 2>);
       case 4: return set(decode_split_kernel<64, 4>);
       case 8: return set(decode_split_kernel<64, 8>);
+      case 16: return set(decode_split_kernel<64, 16>);
     }
   } else {
     switch (G) {
@@ -944,6 +968,7 @@ cudaError_t prepare_decode(const DecodeArgs& p) {
       case 2: return set(decode_split_kernel<128, 2>);
       case 4: return set(decode_split_kernel<128, 4>);
       case 8: return set(decode_split_kernel<128, 8>);
+      case 16: return set(decode_split_kernel<128, 16>);
     }
   }
   return cudaErrorInvalidValue;

@@ -303,7 +303,7 @@ def test_prefill_long_context_chunks(case):
 # ------------------------------------------------------------------ decode kernel coverage
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 8), (32, 16), (64, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 8), (32, 16), (64, 8), (16, 1), (64, 4)])
 @pytest.mark.parametrize("BS", [16, 32, 256])
 def test_decode_heads_and_block_sizes(Hq, Hkv, BS):
     rng = np.random.default_rng(Hq * 100 + Hkv + BS)
@@ -311,6 +311,24 @@ def test_decode_heads_and_block_sizes(Hq, Hkv, BS):
     spec = workloads.custom([1] * len(ctx), ctx, num_q_heads=Hq, num_kv_heads=Hkv,
                             block_size=BS, seed=BS + Hkv)
     full_check(spec)
+
+
+def test_bf16_decode_shapes_run_on_the_tensor_core_kernels():
+    """G = 16 decode (two 8-head column blocks per KV head) runs on the split-KV kernel,
+    not the CUDA-core one."""
+    names = cb.kernel_names()
+    split, portable = names.index("decode_split"), names.index("portable_attention")
+    for Hq, Hkv in ((16, 1), (64, 4)):
+        spec = workloads.custom([1] * 6, [0, 15, 700, 2100, 40, 3000], num_q_heads=Hq,
+                                num_kv_heads=Hkv, seed=Hq + Hkv)
+        st = GpuStep(spec)
+        h = st.host_inputs()
+        s0, p0 = cb.launch_count(split), cb.launch_count(portable)
+        out = st.run()
+        torch.cuda.synchronize()
+        assert cb.launch_count(split) > s0 and cb.launch_count(portable) == p0, (Hq, Hkv)
+        assert cb.read_error_word(st.ws) == 0
+        compare(spec, out, oracle_step(spec, h))
 
 
 @pytest.mark.parametrize("D", [64, 128])
