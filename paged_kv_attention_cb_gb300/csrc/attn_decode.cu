@@ -28,6 +28,8 @@
 //   with four 128B-swizzled TMA tile loads (K and V, two 64-element halves of
 //   D) into a STAGES-deep ring of shared-memory buffers guarded by mbarriers;
 //   the request's query rows arrive by a 1-D bulk copy into a 2-slot ring.
+//   With 8-key pages a block is two pages: two loads of 8 keys each, which
+//   land as rows (page, head, key) instead of (head, key).
 // * Contraction. Per warp and block: S^T (16 keys x 8 heads) = K Q^T and
 //   O^T (D x 8 heads) += V^T P^T on mma.sync m16n8k16 (bf16 in, fp32
 //   accumulate); the key axis is the M dimension so a group of up to 8 query
@@ -78,6 +80,13 @@ struct DecodeSmem {
 CB_DEV int kb_lo_of(int seq, int window) {
   const int lo = window > 0 ? max(0, seq - window) : 0;
   return lo / kKB;
+}
+
+// Row of (local head hl, key k of the 16-key block) in a staged K or V half: (head, key)
+// for pages of 16 keys or more, (page, head, key) for 8-key pages. Rows are 128 bytes
+// and the 128B swizzle depends on the row's index modulo 8, which is k mod 8 either way.
+CB_DEV int stage_row(bool pages8, int hb, int hl, int k) {
+  return pages8 ? ((k >> 3) * hb + hl) * 8 + (k & 7) : hl * kKB + k;
 }
 
 // Key blocks a decode query of a request of seq_len `seq` attends.
@@ -277,11 +286,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       return R;
     };
-    auto load_pages = [&](int r, int kb_start, int n) -> int {
+    const bool pages8 = p.a.block_size < kKB;  // 8-key pages: two per key block
+    // page id(s) of key block kb_start + lane (lane < n): with 8-key pages the block's
+    // second page goes to pg2 (-1 past the request's last page, whose table entry may
+    // not exist)
+    int pg2_next = -1;
+    auto load_pages = [&](int r, int kb_start, int n, int seq_r) -> int {
       int pg = 0;
-      if (lane < n)
-        pg = __ldg(p.a.block_table + (long long)r * p.a.bt_stride +
-                   bt_entry((kb_start + lane) * kKB / p.a.block_size, p.a.ring_blocks));
+      pg2_next = -1;
+      if (lane < n) {
+        const int32_t* row = p.a.block_table + (long long)r * p.a.bt_stride;
+        const int lp = (kb_start + lane) * kKB / p.a.block_size;
+        pg = __ldg(row + bt_entry(lp, p.a.ring_blocks));
+        if (pages8 && (lp + 1) * p.a.block_size < seq_r)
+          pg2_next = __ldg(row + bt_entry(lp + 1, p.a.ring_blocks));
+      }
       return pg;
     };
     // walk state of the current segment
@@ -295,6 +314,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     };
     int kb0 = 0, kb1 = 0;
     int pages = 0;  // page ids of the batch about to be issued (lane j: key block kb + j)
+    int pages2 = -1;  // 8-key pages: the block's second page
     if (u_lo < u_hi && sm.first_r >= 0) {
       r = sm.first_r;
       u_r = sm.first_u;
@@ -307,7 +327,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         t = c.t;
         seq = c.seq;
         units = units_of(seq, p.a.sliding_window);
-        pages = load_pages(r, kb0, min(32, kb1 - kb0));
+        pages = load_pages(r, kb0, min(32, kb1 - kb0), seq);
+        pages2 = pg2_next;
         load_window(r);
       } else {
         load_window(r);
@@ -315,7 +336,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int kbl = kb_lo_of(seq, p.a.sliding_window);
         kb0 = kbl + (int)(u - u_r);
         kb1 = kbl + (int)(min(u_r + units, u_hi) - u_r);
-        pages = load_pages(r, kb0, min(32, kb1 - kb0));
+        pages = load_pages(r, kb0, min(32, kb1 - kb0), seq);
+        pages2 = pg2_next;
       }
     }
     if (p.metadata_ready) grid_dependency_wait();  // the scatter must be complete
@@ -357,9 +379,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       };
       for (int kb_base = kb0; kb_base < kb1 && ok; kb_base += 32) {
         const int nkb = min(32, kb1 - kb_base);
-        const int cur = pages;
+        const int cur = pages, cur2 = pages2;
         for (int j = 0; j < nkb; ++j) {
           const int pg = __shfl_sync(0xffffffffu, cur, j);
+          const int pg2 = __shfl_sync(0xffffffffu, cur2, j);
           const int kb = kb_base + j;
           const int s = (int)(i % p.stages);
           if (i >= p.stages && !mbar_wait_warp_or_abort(&sm.empty[s],
@@ -375,7 +398,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
               record_error(p.a.error_word, CB_DEVERR_BLOCK_ID_CODE);
               pgc = p.a.num_blocks;  // TMA reads past the pool as zeros
             }
-            const int key0 = (kb * kKB) % p.a.block_size;
+            const int key0 = pages8 ? 0 : (kb * kKB) % p.a.block_size;
             uint8_t* st = stages + s * p.stage_bytes;
             mbar_arrive_expect_tx(&sm.full[s], (uint32_t)p.stage_bytes);
 #pragma unroll
@@ -385,6 +408,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
               tma_load_4d_hint(st + (kHalves + h) * box_bytes, &tmap_v, &sm.full[s], h * 64,
                                key0, hg * HB, pgc, kv_policy);
             }
+            if (pages8) {
+              // the block's keys 8-15: the next page (past the request: zeros; its keys
+              // are masked and its V rows zeroed by the consumers)
+              int pgc2 = pg2;
+              if (pg2 >= p.a.num_blocks) {
+                record_error(p.a.error_word, CB_DEVERR_BLOCK_ID_CODE);
+                pgc2 = p.a.num_blocks;
+              } else if (pg2 < 0) {
+                pgc2 = p.a.num_blocks;
+              }
+              const int half8 = HB * 8 * 128;  // rows (page 1, head, key) start here
+#pragma unroll
+              for (int h = 0; h < kHalves; ++h) {
+                tma_load_4d_hint(st + h * box_bytes + half8, &tmap_k, &sm.full[s], h * 64, 0,
+                                 hg * HB, pgc2, kv_policy);
+                tma_load_4d_hint(st + (kHalves + h) * box_bytes + half8, &tmap_v, &sm.full[s],
+                                 h * 64, 0, hg * HB, pgc2, kv_policy);
+              }
+            }
           }
           __syncwarp();
           ++i;
@@ -392,7 +434,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // page ids of the batch after this one: the rest of this segment, or the
             // next segment's start
             if (kb_base + 32 < kb1) {
-              pages = load_pages(r, kb_base + 32, min(32, kb1 - kb_base - 32));
+              pages = load_pages(r, kb_base + 32, min(32, kb1 - kb_base - 32), seq);
+              pages2 = pg2_next;
             } else {
               lookup_next();
               if (nr >= 0) {
@@ -402,7 +445,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int nkbl = kb_lo_of(n_seq, p.a.sliding_window);
                 nkb0 = nkbl;
                 nkb1 = nkbl + (int)(min(nu_r + n_units, u_hi) - nu_r);
-                pages = load_pages(nr, nkb0, min(32, nkb1 - nkb0));
+                pages = load_pages(nr, nkb0, min(32, nkb1 - nkb0), n_seq);
+                pages2 = pg2_next;
               }
             }
           }
@@ -440,6 +484,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // the CTA's final barrier)
   auto consume = [&]() {
   const int hl = warp;  // local KV head
+  const bool pages8 = p.a.block_size < kKB;
   constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's K (or V) row
   const long long num_slots = (long long)p.a.num_blocks * p.a.block_size;
   const int gid = lane >> 2;
@@ -528,7 +573,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int c = lane % kRowChunks;
             const int key = d.hi - key_base;
             uint8_t* tile = lane < kRowChunks ? ks_base : vs_base;
-            *reinterpret_cast<uint4*>(tile + (c >> 3) * box_bytes + (hl * kKB + key) * 128 +
+            *reinterpret_cast<uint4*>(tile + (c >> 3) * box_bytes + stage_row(pages8, HB, hl, key) * 128 +
                                       (((c & 7) ^ (key & 7)) << 4)) = new_row;
             uint4* cache = static_cast<uint4*>(lane < kRowChunks ? p.a.k_cache : p.a.v_cache);
             cache[(row_slot * p.a.num_kv_heads + hg * HB + hl) * kRowChunks + c] = new_row;
@@ -550,8 +595,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
           const int rem = e % (kHalves * 8);
           const int h = rem >> 3;
           const int c = rem & 7;
-          *reinterpret_cast<uint4*>(vs_base + h * box_bytes + (hl * kKB + row) * 128 + c * 16) =
-              make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vs_base + h * box_bytes + stage_row(pages8, HB, hl, row) * 128 +
+                                    c * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();  // as above: before the stage is handed back to the copies
         __syncwarp();
@@ -563,7 +608,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       {
         const int jm = lane >> 3;
         const int key = (lane & 7) + ((jm & 1) << 3);
-        const uint32_t row_addr = smem_u32(ks_base) + (hl * kKB + key) * 128;
+        const uint32_t row_addr = smem_u32(ks_base) + stage_row(pages8, HB, hl, key) * 128;
 #pragma unroll
         for (int ks = 0; ks < kKSteps; ++ks) {
           const int chunk = (ks & 3) * 2 + (jm >> 1);
@@ -613,7 +658,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
       {
         const int jm = lane >> 3;
         const int key = (lane & 7) + ((jm >> 1) << 3);
-        const uint32_t row_addr = smem_u32(vs_base) + (hl * kKB + key) * 128;
+        const uint32_t row_addr = smem_u32(vs_base) + stage_row(pages8, HB, hl, key) * 128;
 #pragma unroll
         for (int m = 0; m < kKSteps; ++m) {
           const int chunk = 2 * m + (jm & 1);
@@ -876,7 +921,8 @@ cudaError_t make_cache_map(CUtensorMap* map, void* cache, const StepArgs& a, int
   cuuint64_t strides[3] = {(cuuint64_t)a.num_kv_heads * a.head_dim * elt,
                            (cuuint64_t)a.head_dim * elt,
                            (cuuint64_t)a.block_size * a.num_kv_heads * a.head_dim * elt};
-  cuuint32_t box[4] = {64, 16, (cuuint32_t)hb, 1};
+  // 16 keys of one page, or all 8 of an 8-key page (a block then takes two boxes)
+  cuuint32_t box[4] = {64, (cuuint32_t)(a.block_size < 16 ? a.block_size : 16), (cuuint32_t)hb, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, cache, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

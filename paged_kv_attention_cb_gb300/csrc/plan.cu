@@ -166,7 +166,8 @@ void plan_step(Plan& plan, const StepArgs& a, const int32_t* h_qsl, const int32_
   // ---- which kernels can take them
   const int G = a.num_q_heads / a.num_kv_heads;
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
-  const bool decode_ok = U > 0 && a.block_size % 16 == 0 && G <= 16 && a.num_kv_heads % HB == 0;
+  const bool decode_ok = U > 0 && (a.block_size % 16 == 0 || a.block_size == 8) && G <= 16 &&
+                         a.num_kv_heads % HB == 0;
   // a 128-key tile is made of whole page boxes (block_size divides 128) or lies
   // inside one page (block_size a multiple of 128)
   const bool tile_pages_ok = a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
@@ -336,7 +337,8 @@ bool plan_graph_step(Plan& plan, const StepArgs& a, bool with_decode, bool with_
   const int HB = std::min(a.num_kv_heads, kDecodeMaxHeads);
   const bool tile_pages_ok =
       a.block_size % 8 == 0 && (128 % a.block_size == 0 || a.block_size % 128 == 0);
-  if (!(a.block_size % 16 == 0 && G <= 16 && a.num_kv_heads % HB == 0)) return false;
+  if (!((a.block_size % 16 == 0 || a.block_size == 8) && G <= 16 && a.num_kv_heads % HB == 0))
+    return false;
   if (!(tile_pages_ok && G <= 16 && kRowsPerTile % G == 0)) return false;
 
   DecodeArgs& d = plan.decode;

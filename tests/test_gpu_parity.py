@@ -304,7 +304,7 @@ def test_prefill_long_context_chunks(case):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 8), (32, 16), (64, 8), (16, 1), (64, 4)])
-@pytest.mark.parametrize("BS", [16, 32, 256])
+@pytest.mark.parametrize("BS", [8, 16, 32, 256])
 def test_decode_heads_and_block_sizes(Hq, Hkv, BS):
     rng = np.random.default_rng(Hq * 100 + Hkv + BS)
     ctx = [int(c) for c in rng.integers(0, 3000, size=12)] + [0, 15, 16, 31]
@@ -314,19 +314,19 @@ def test_decode_heads_and_block_sizes(Hq, Hkv, BS):
 
 
 def test_bf16_decode_shapes_run_on_the_tensor_core_kernels():
-    """G = 16 decode (two 8-head column blocks per KV head) runs on the split-KV kernel,
-    not the CUDA-core one."""
+    """G = 16 decode (two 8-head column blocks per KV head) and 8-key pages (two page
+    boxes per 16-key block) run on the split-KV kernel, not the CUDA-core one."""
     names = cb.kernel_names()
     split, portable = names.index("decode_split"), names.index("portable_attention")
-    for Hq, Hkv in ((16, 1), (64, 4)):
+    for Hq, Hkv, BS in ((16, 1, 16), (64, 4, 16), (32, 8, 8), (16, 1, 8)):
         spec = workloads.custom([1] * 6, [0, 15, 700, 2100, 40, 3000], num_q_heads=Hq,
-                                num_kv_heads=Hkv, seed=Hq + Hkv)
+                                num_kv_heads=Hkv, block_size=BS, seed=Hq + Hkv + BS)
         st = GpuStep(spec)
         h = st.host_inputs()
         s0, p0 = cb.launch_count(split), cb.launch_count(portable)
         out = st.run()
         torch.cuda.synchronize()
-        assert cb.launch_count(split) > s0 and cb.launch_count(portable) == p0, (Hq, Hkv)
+        assert cb.launch_count(split) > s0 and cb.launch_count(portable) == p0, (Hq, Hkv, BS)
         assert cb.read_error_word(st.ws) == 0
         compare(spec, out, oracle_step(spec, h))
 
