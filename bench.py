@@ -1273,6 +1273,14 @@ def workload_summary(spec, res, world):
             "peak_source": f"{tkind} dense bf16 (burst: the kernel is timed alone)",
             "algorithmic_flops_per_launch": fl, "avg_launch_ms": pms,
             "traffic": recorded_traffic("prefill_tc", spec.name)}
+        if "decode_split" in pk:
+            # the whole step's bound with the two parts one after the other at their peaks:
+            # every byte at the measured HBM bandwidth plus every FLOP at the bf16 peak
+            t_star = (kvb / (peak * 1e9) + fl / (tpk * 1e12)) * 1e3
+            line["step_bound"] = {"t_star_ms": t_star, "step_ms": ms, "t_star_over_step": t_star / ms,
+                                  "what": "algorithmic KV bytes / measured HBM + prefill FLOPs / "
+                                          "measured bf16 peak (the kernels run side by side, "
+                                          "so the step can beat it)"}
     line["clocks"] = res["clocks"]
     return line
 
