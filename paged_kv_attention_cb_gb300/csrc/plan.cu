@@ -112,7 +112,7 @@ int prefill_sm_share(long long decode_bytes, double prefill_flops, int n_prefill
   if (env != nullptr && *env != '\0') return std::max(1, std::min(atoi(env), kmax));
   constexpr double kHbm = 6.6e12;          // B/s, decode stream on enough SMs
   constexpr double kHbmPerSm = 75e9;       // B/s, decode stream per SM
-  constexpr double kFlopsPerSm = 6.0e12;   // causal-pair FLOP/s of prefill tiles per SM
+  constexpr double kFlopsPerSm = 7.0e12;   // causal-pair FLOP/s of prefill tiles per SM
   int best_k = 1;
   double best_t = 1e30;
   for (int k = 1; k <= kmax; ++k) {
