@@ -166,8 +166,9 @@ struct Work {
   int e, g, pair;
 };
 
-// CTA -> (entry, KV head, pair of query tiles); entries are sorted heaviest
-// first and each request's pairs are taken last first (the last has the most keys).
+// Unit index of the step's list -> (entry, KV head, pair of query tiles); entries are
+// sorted heaviest first and each request's pairs are taken last first (the last has the
+// most keys), so the list runs heaviest first.
 CB_DEV Work work_of(const PrefillArgs& p, int cta) {
   const int Hkv = p.a.num_kv_heads;
   int base = 0;

@@ -30,9 +30,9 @@ struct PrefillArgs {
   // The step's new K/V rows (nullptr: none, or already in the cache). With them the
   // kernel reads a request's own new positions from k_new / v_new instead of the
   // cache -- each position whose slot_mapping entry is its own slot, which is the
-  // value the cache will hold -- and CTA (request, KV head, tile pair) writes the rows
-  // of its tokens and head into their slots, so the step needs no scatter launch and
-  // nothing in it reads a position written in it.
+  // value the cache will hold -- and its CTAs copy the rows of every listed request
+  // into their slots (claimed in parts once their units are done), so the step needs no
+  // scatter launch and nothing in it reads a position written in it.
   const void* k_new;
   const void* v_new;
   const int64_t* slot_mapping;
