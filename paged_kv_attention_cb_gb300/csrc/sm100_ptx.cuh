@@ -329,6 +329,26 @@ CB_DEV float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Packed fp32 pairs (sm_100 family): one instruction for two lanes' worth of work, which
+// halves the issue slots of the softmax's exponent arguments and row sums.
+// (d0, d1) = (a0, a1) * b + c, round to nearest
+CB_DEV void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  unsigned long long dd, aa, bb, cc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(dd) : "l"(aa), "l"(bb), "l"(cc));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(dd));
+}
+// (s0, s1) += (a0, a1), round to nearest
+CB_DEV void fadd2(float& s0, float& s1, float a0, float a1) {
+  unsigned long long ss, aa, dd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ss) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(aa) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(dd) : "l"(ss), "l"(aa));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(dd));
+}
+
 CB_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
