@@ -184,6 +184,60 @@ CB_DEV Work work_of(const PrefillArgs& p, int cta) {
   return Work{-1, 0, 0};
 }
 
+// The pages of key tile `key_base` in `gen` (bit i: page i of the tile), row by row into
+// the ring slot `dst` (128B-swizzled rows of 64 of head_dim per half): a new position whose
+// slot is its own (bit clear in `bad`) from the step's new rows, any other from its cache
+// page; positions past the request as zeros. Out of line: the path is rare (pages that
+// straddle the context end or hold a foreign slot), and kept inline its registers and code
+// slowed the TMA warps' common path (~3% of a long unit's key loop).
+template <int D>
+__device__ __noinline__ void copy_rows(uint8_t* dst, unsigned gen, int ids_cur, unsigned bad0,
+                                       unsigned bad1, unsigned bad2, unsigned bad3, int key_base, int ctx, int seq, int q_start, int g, int Hkv,
+                                       int BS, int box, const uint4* new_rows, const uint4* cache,
+                                       int num_blocks, int32_t* error_word) {
+  constexpr int kHalves = D / 64;
+  constexpr int kBatch = 4;  // 16-byte chunks e = lane + 32 m of (row, half, chunk), loads first
+  const int lane = threadIdx.x & 31;
+  const int bs_mask = BS - 1;
+  for (unsigned m = gen; m != 0u; m &= m - 1u) {
+    const int pi = __ffs(m) - 1;
+    const int pg = __shfl_sync(0xffffffffu, ids_cur, pi);
+    const int kpi = key_base + pi * box;
+    const bool pg_ok = pg >= 0 && pg < num_blocks;
+    const int nchunks = box * kHalves * 8;
+    for (int e0 = 0; e0 < nchunks; e0 += 32 * kBatch) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + lane + 32 * u;
+        const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+        const int pos = kpi + row;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < nchunks && pos < seq) {
+          const int kk = pos - key_base;
+          const unsigned bw = kk < 32 ? bad0 : kk < 64 ? bad1 : kk < 96 ? bad2 : bad3;
+          const bool own = pos >= ctx && ((bw >> (kk & 31)) & 1u) == 0u;
+          if (own) {
+            v[u] = __ldg(new_rows + (((long long)(q_start + pos - ctx) * Hkv + g) * D + h * 64) / 8 + c);
+          } else if (pg_ok) {
+            v[u] = __ldg(cache + (((long long)pg * BS + (pos & bs_mask)) * Hkv + g) * (D / 8) + h * 8 + c);
+          } else if (c == 0 && h == 0) {
+            record_error(error_word, 0x1);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + lane + 32 * u;
+        const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
+        const int trow = pi * box + row;  // row within the tile
+        if (e < nchunks)
+          *reinterpret_cast<uint4*>(dst + h * kHalfBytes + trow * 128 + ((c ^ (trow & 7)) << 4)) = v[u];
+      }
+    }
+  }
+}
+
 }  // namespace
 
 template <int D>
@@ -508,45 +562,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
           gen = __ballot_sync(0xffffffffu, src == 2);
         }
         if (gen != 0u) {
-          // row by row: 16-byte chunks e = lane + 32 m of (row, half, chunk), loads first
-          constexpr int kBatch = 8;
-          for (unsigned m = gen; m != 0u; m &= m - 1u) {
-            const int pi = __ffs(m) - 1;
-            const int pg = __shfl_sync(0xffffffffu, ids_cur, pi);
-            const int kpi = key_base + pi * box;
-            const bool pg_ok = pg >= 0 && pg < p.a.num_blocks;
-            const int nchunks = box * kHalves * 8;
-            for (int e0 = 0; e0 < nchunks; e0 += 32 * kBatch) {
-              uint4 v[kBatch];
-#pragma unroll
-              for (int u = 0; u < kBatch; ++u) {
-                const int e = e0 + lane + 32 * u;
-                const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
-                const int pos = kpi + row;
-                v[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (e < nchunks && pos < seq) {
-                  const int kk = pos - key_base;
-                  const unsigned bw = kk < 32 ? bad[0] : kk < 64 ? bad[1] : kk < 96 ? bad[2] : bad[3];
-                  const bool own = pos >= ctx && ((bw >> (kk & 31)) & 1u) == 0u;
-                  if (own) {
-                    v[u] = __ldg(new_rows + (((long long)(q_start + pos - ctx) * Hkv + g) * D + h * 64) / 8 + c);
-                  } else if (pg_ok) {
-                    v[u] = __ldg(cache + (((long long)pg * BS + (pos & bs_mask)) * Hkv + g) * (D / 8) + h * 8 + c);
-                  } else if (c == 0 && h == 0) {
-                    record_error(p.a.error_word, 0x1);
-                  }
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < kBatch; ++u) {
-                const int e = e0 + lane + 32 * u;
-                const int row = e / (kHalves * 8), h = (e / 8) % kHalves, c = e % 8;
-                const int trow = pi * box + row;  // row within the tile
-                if (e < nchunks)
-                  *reinterpret_cast<uint4*>(dst + h * kHalfBytes + trow * 128 + ((c ^ (trow & 7)) << 4)) = v[u];
-              }
-            }
-          }
+          copy_rows<D>(dst, gen, ids_cur, bad[0], bad[1], bad[2], bad[3], key_base, ctx, seq, q_start, g,
+                       Hkv, BS, box, new_rows, cache, p.a.num_blocks, p.a.error_word);
           // the tensor cores read these rows through the async proxy
           fence_proxy_async_smem();
           __syncwarp();
