@@ -877,28 +877,67 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         ok = false;
       const Geo e = CB_UNIT_GEO();
       const int g = e.g, q_start = e.q_start;
-      const int tok = (e.qt0 + t) * TQ + row / G;
-      const int hh = row % G;
-      const bool row_valid = tok < e.q_len;
       if (ok) {
         tcgen05_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.a.out) +
-                              ((long long)(q_start + tok) * p.a.num_q_heads + g * G + hh) * D;
+        // O / l as bf16 in whole 128-byte lines. Each lane holds its own row (TMEM lane =
+        // row); a transpose of 32-byte pieces within each group of four lanes gives lane
+        // 4a + q piece q of rows 4a .. 4a + 3 of the warp, so that one store instruction
+        // writes 8 rows x 128 contiguous bytes instead of 32 rows x 16 bytes (the stores of
+        // one row per lane kept the LSU busy ~4000 cycles per unit).
+        const int q4 = lane & 3;
+        const bool wide = (reinterpret_cast<uintptr_t>(p.a.out) & 31) == 0;
+        long long orow[4];  // bf16 offset of rows 4a .. 4a + 3 of the warp, -1 past q_len
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o32[32];
-          tmem_ld32(tO + c0, o32);
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int r = (warp & 3) * 32 + 4 * (lane >> 2) + s4;  // tile row
+          const int tok = (e.qt0 + t) * TQ + r / G;
+          orow[s4] = tok < e.q_len
+                         ? ((long long)(q_start + tok) * p.a.num_q_heads + g * G + r % G) * D + q4 * 16
+                         : -1;
+        }
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out);
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO + c0, o0);
+          tmem_ld32(tO + c0 + 32, o1);
           tmem_wait_ld();
-          if (row_valid) {
+          uint32_t w[32];  // piece k = words 8k .. 8k + 7 = columns c0 + 16k .. c0 + 16k + 15
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 0]) * inv, __uint_as_float(o32[c8 * 8 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 2]) * inv, __uint_as_float(o32[c8 * 8 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 4]) * inv, __uint_as_float(o32[c8 * 8 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(o32[c8 * 8 + 6]) * inv, __uint_as_float(o32[c8 * 8 + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c0 + c8 * 8) = v;
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+            w[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+          }
+          // in-quad transpose: at lane distance d, the lane whose bit d is set swaps its
+          // pieces with bit d clear for its partner's pieces with bit d set
+#pragma unroll
+          for (int d = 2; d >= 1; d >>= 1) {
+            const bool hi = (lane & d) != 0;
+#pragma unroll
+            for (int k0 = 0; k0 < 4; ++k0) {
+              if (k0 & d) continue;
+              const int k1 = k0 | d;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t x = hi ? w[8 * k0 + i] : w[8 * k1 + i];
+                const uint32_t y = __shfl_xor_sync(0xffffffffu, x, d);
+                if (hi) w[8 * k0 + i] = y;
+                else w[8 * k1 + i] = y;
+              }
+            }
+          }
+          // now piece s4 of this lane = columns c0 + 16 q .. + 15 of row 4a + s4
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            if (orow[s4] < 0) continue;
+            __nv_bfloat16* dst = out + orow[s4] + c0;
+            if (wide) {
+              st_global_v8(dst, w[8 * s4 + 0], w[8 * s4 + 1], w[8 * s4 + 2], w[8 * s4 + 3],
+                           w[8 * s4 + 4], w[8 * s4 + 5], w[8 * s4 + 6], w[8 * s4 + 7]);
+            } else {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(w[8 * s4 + 0], w[8 * s4 + 1], w[8 * s4 + 2], w[8 * s4 + 3]);
+              *reinterpret_cast<uint4*>(dst + 8) = make_uint4(w[8 * s4 + 4], w[8 * s4 + 5], w[8 * s4 + 6], w[8 * s4 + 7]);
             }
           }
         }

@@ -404,6 +404,31 @@ def test_prefill_fast_equals_portable_path():
     assert float(err.max()) <= 2e-2 and float(err.mean()) <= 2e-3
 
 
+@pytest.mark.parametrize("D,G", [(128, 4), (64, 8), (128, 1), (128, 16)])
+def test_prefill_output_at_a_16_byte_offset_equals_aligned(D, G):
+    """The prefill kernel writes O in 32-byte pieces where `out` is 32-byte aligned and in
+    16-byte ones otherwise (the boundary asks for 16-byte alignment only): both give the
+    same bits, every row of every request is written (the buffers start as NaN) and nothing
+    past the last request's last token (a ragged tile) or before the output."""
+    spec = workloads.custom([37, 300, 5, 129], [0, 200, 90, 7], num_q_heads=2 * G,
+                            num_kv_heads=2, head_dim=D, seed=23)
+    st = GpuStep(spec)
+    h = st.host_inputs()
+    aligned = st.run()
+    assert aligned.data_ptr() % 32 == 0
+    n, guard = aligned.numel(), 4096
+    buf = torch.full((8 + n + guard,), float("nan"), dtype=aligned.dtype, device=aligned.device)
+    shifted = buf[8:8 + n].view(aligned.shape)
+    assert shifted.data_ptr() % 32 == 16
+    st.run(out=shifted)
+    torch.cuda.synchronize()
+    assert cb.read_error_word(st.ws) == 0
+    assert not torch.isnan(aligned.float()).any()
+    assert torch.equal(aligned.view(torch.int16), shifted.view(torch.int16))
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all()
+    compare(spec, aligned, oracle_step(spec, h))
+
+
 # ------------------------------------------------------------------ ring-recycled sliding pages
 
 
