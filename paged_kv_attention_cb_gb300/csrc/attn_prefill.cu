@@ -264,7 +264,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int Hkv = p.a.num_kv_heads;
-  const int G = p.a.num_q_heads / Hkv;
+  const int G = p.a.num_q_heads / Hkv;  // divides 128 (the launch checks): a power of two
   const int TQ = p.tile_tokens;
   const int W = p.a.sliding_window;
   // Graph replays: the one unit of this CTA, found with a block scan over the device
@@ -726,6 +726,9 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tO = tmem + lane_addr + 2 * kKeys + t * D;
     int i_base = 0;
     int swaits = 0;  // s_full[t] waits so far (phase parity)
+    const bool copy_rows_after = p.k_new != nullptr && !p.device_work;  // the row copy below
+    bool claimed = false;  // its first part is claimed already (lane 0: first_part)
+    int first_part = 0;
     int owaits = 0;  // o_done[t] waits so far
     for (int u = 0; ok; ++u) {
       // The unit stays in its ring slot until this group is done with it (the slot is
@@ -872,11 +875,36 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar.p_full[t]);
       }
-      // ---- epilogue: O / l for the rows of this tile
+      // ---- epilogue: O / l for the rows of this tile. The rows' output offsets are
+      // computed while the last PV product runs (~600 cycles after the wait otherwise).
+      const int q4 = lane & 3;
+      long long orow[4];  // bf16 offset of rows 4a .. 4a + 3 of the warp, -1 past q_len
+      {
+        const Geo e = CB_UNIT_GEO();
+        const int lg = __ffs(G) - 1;
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int r = (warp & 3) * 32 + 4 * (lane >> 2) + s4;  // tile row
+          const int tok = (e.qt0 + t) * TQ + (r >> lg);
+          orow[s4] = tok < e.q_len ? ((long long)(e.q_start + tok) * p.a.num_q_heads + e.g * G +
+                                      (r & (G - 1))) * D + q4 * 16
+                                   : -1;
+        }
+      }
+      // When the next unit is already published as the end of the list, the first part of
+      // the row copy that follows is claimed now: the claim's round trip to L2 overlaps
+      // the epilogue instead of following it on the CTA's last unit.
+      if (copy_rows_after && !claimed) {
+        int last = 0;
+        if (lane == 0 && mbar_try_wait(&bar.unit_full[(u + 1) & 1], (uint32_t)(((u + 1) >> 1) & 1)) &&
+            !bar.unit[(u + 1) & 1].live) {
+          last = 1;
+          first_part = atomicAdd(p.scatter_counter, 1);
+        }
+        claimed = __shfl_sync(0xffffffffu, last, 0) != 0;
+      }
       if (ok && !mbar_wait_warp_or_abort(&bar.o_done[t], (uint32_t)(owaits++ & 1), &bar.abort))
         ok = false;
-      const Geo e = CB_UNIT_GEO();
-      const int g = e.g, q_start = e.q_start;
       if (ok) {
         tcgen05_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -885,17 +913,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // 4a + q piece q of rows 4a .. 4a + 3 of the warp, so that one store instruction
         // writes 8 rows x 128 contiguous bytes instead of 32 rows x 16 bytes (the stores of
         // one row per lane kept the LSU busy ~4000 cycles per unit).
-        const int q4 = lane & 3;
         const bool wide = (reinterpret_cast<uintptr_t>(p.a.out) & 31) == 0;
-        long long orow[4];  // bf16 offset of rows 4a .. 4a + 3 of the warp, -1 past q_len
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int r = (warp & 3) * 32 + 4 * (lane >> 2) + s4;  // tile row
-          const int tok = (e.qt0 + t) * TQ + r / G;
-          orow[s4] = tok < e.q_len
-                         ? ((long long)(q_start + tok) * p.a.num_q_heads + g * G + r % G) * D + q4 * 16
-                         : -1;
-        }
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out);
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 64) {
@@ -965,7 +983,7 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // tokens for its KV head at a time, so that it runs while the longest units compute
     // and competes with no product of its own CTA. The parts of all units cover every
     // (token, KV head) of the listed requests once.
-    if (ok && p.k_new != nullptr && !p.device_work) {
+    if (ok && copy_rows_after) {
       constexpr int kParts = 4;
       constexpr int kRowChunks = D / 8;  // 16-byte chunks of one head's row
       constexpr int kPerTok = 2 * kRowChunks;
@@ -979,7 +997,8 @@ prefill_tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
       const int n_parts = p.total_units * kParts;
       for (;;) {
         int it = 0;
-        if (lane == 0) it = atomicAdd(p.scatter_counter, 1);
+        if (lane == 0) it = claimed ? first_part : atomicAdd(p.scatter_counter, 1);
+        claimed = false;
         it = __shfl_sync(0xffffffffu, it, 0);
         if (it >= n_parts) break;
         const Work w = work_of(p, it / kParts);
@@ -1079,6 +1098,7 @@ cudaError_t launch_d(const PrefillArgs& p, cudaStream_t s) {
   CUtensorMap mq;
   {
     const int G = a.num_q_heads / a.num_kv_heads;
+    if (G < 1 || kRows % G != 0 || p.tile_tokens != kRows / G) return cudaErrorInvalidValue;
     cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
     cuuint64_t qs[2] = {(cuuint64_t)D * e, (cuuint64_t)a.num_q_heads * D * e};
     cuuint32_t qb[3] = {64, (cuuint32_t)G, (cuuint32_t)p.tile_tokens};
