@@ -44,7 +44,8 @@
 //   tensor pipe runs the other group's products, so exponentials and MMAs
 //   overlap. The running maximum is only raised (and O rescaled in TMEM) when
 //   it grows by more than 2^8, which keeps every P <= 256 and the result exact
-//   up to rounding. After the last PV, O is divided by the row sum and written.
+//   up to rounding. After the last PV, O is divided by the row sum and written
+//   in whole 128-byte lines (32-byte pieces transposed within groups of four lanes).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <float.h>
